@@ -1,0 +1,204 @@
+"""Pins for the CPU oracle: checks fixed by the definition of GEMM and by arithmetic,
+not by the oracle itself. Each pin takes the oracle's ctypes handle, so the same checks
+run against the real oracle (all must pass) and against deliberately broken copies of it
+(each copy must fail at least one).
+
+Sources of each pin:
+* identity / permutation: A.I = A, I.B = B, P.B permutes rows of B, A.P permutes columns
+  of A, exactly; the definition of each cell as a row-column dot product ("GEMM scrapbook",
+  GEMM definition; "The 1% kernel", section 1).
+* all-ones: a dot product of K ones with K ones is K.
+* small integers: with |entries| <= 4 and K <= 16384 every partial sum is an integer below
+  2**24, exact in any order, so the result equals the int64 product (numpy integer matmul,
+  a separate routine) exactly.
+* alpha/beta: C = alpha*(A.B) + beta*C ("a CUDA matmul", section 00) with the BLAS readings
+  for beta = 0 (C not read), alpha = 0 (A, B not read) and K = 0.
+* cancellation: terms exactly representable in fp32 whose running sum needs more than 24
+  bits; the exact sum is representable, so one final rounding reproduces it.
+* brute force: exact rational arithmetic (fractions.Fraction) on tiny shapes, rounded once
+  to fp32; the oracle may differ by at most one fp32 ulp (its fp64 sum rounds before the
+  final rounding).
+"""
+from __future__ import annotations
+
+import itertools
+from fractions import Fraction
+
+import numpy as np
+
+import oracle
+import synth
+
+
+def _mm(lib, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, rows=None):
+    return oracle.sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, rows=rows, lib=lib)
+
+
+def pin_identity(lib):
+    for (M, K) in [(7, 7), (5, 9), (33, 17)]:
+        A = synth.uniform(M, K, 11)
+        eye = np.eye(K, dtype=np.float32)
+        if not np.array_equal(_mm(lib, M, K, K, 1.0, A, K, eye, K, 0.0, None, K), A):
+            return False
+        B = synth.uniform(M, K, 12)  # M x K used as a K'=M rows matrix
+        eyeM = np.eye(M, dtype=np.float32)
+        if not np.array_equal(_mm(lib, M, K, M, 1.0, eyeM, M, B, K, 0.0, None, K), B):
+            return False
+    return True
+
+
+def pin_permutation(lib):
+    rng = np.random.default_rng(3)
+    for (M, K, N) in [(6, 6, 6), (9, 5, 4), (4, 11, 13)]:
+        p = rng.permutation(K)
+        P = np.zeros((K, K), dtype=np.float32)
+        P[np.arange(K), p] = 1.0                      # (P.B)[r] = B[p[r]]
+        B = synth.uniform(K, N, 21)
+        if not np.array_equal(_mm(lib, K, N, K, 1.0, P, K, B, N, 0.0, None, N), B[p]):
+            return False
+        A = synth.uniform(M, K, 22)
+        # (A.P)[:, c] = sum_r A[:, r] P[r, c] = A[:, p^-1(c)]
+        inv = np.argsort(p)
+        if not np.array_equal(_mm(lib, M, K, K, 1.0, A, K, P, K, 0.0, None, K), A[:, inv]):
+            return False
+    return True
+
+
+def pin_all_ones(lib):
+    for (M, N, K) in [(3, 5, 1), (4, 3, 7), (2, 2, 4097), (3, 2, 16384)]:
+        A = np.ones((M, K), dtype=np.float32)
+        B = np.ones((K, N), dtype=np.float32)
+        out = _mm(lib, M, N, K, 1.0, A, K, B, N, 0.0, None, N)
+        if not np.array_equal(out, np.full((M, N), K, dtype=np.float32)):
+            return False
+    return True
+
+
+def pin_small_int(lib):
+    for (M, N, K, seed) in [(5, 7, 3, 0), (17, 13, 129, 1), (8, 9, 4099, 2), (3, 4, 16384, 3)]:
+        A = synth.small_int(M, K, seed)
+        B = synth.small_int(K, N, seed + 1)
+        C = synth.small_int(M, N, seed + 2)
+        exact = A.astype(np.int64) @ B.astype(np.int64)
+        if not np.array_equal(_mm(lib, M, N, K, 1.0, A, K, B, N, 0.0, None, N),
+                              exact.astype(np.float32)):
+            return False
+        # alpha = 2, beta = -3: still exact (|value| < 2**24)
+        want = (2 * exact - 3 * C.astype(np.int64)).astype(np.float32)
+        if not np.array_equal(_mm(lib, M, N, K, 2.0, A, K, B, N, -3.0, C, N), want):
+            return False
+    return True
+
+
+def pin_alpha_beta(lib):
+    M, N, K = 6, 5, 4
+    A = synth.small_int(M, K, 5)
+    B = synth.small_int(K, N, 6)
+    C = synth.small_int(M, N, 7)
+    S = (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float64)
+    # beta = 0 ignores C, even NaN / Inf there
+    Cbad = C.copy()
+    Cbad[0, 0], Cbad[1, 1], Cbad[2, 3] = np.nan, np.inf, -np.inf
+    out = _mm(lib, M, N, K, 1.5, A, K, B, N, 0.0, Cbad, N)
+    if not np.array_equal(out, (1.5 * S).astype(np.float32)):
+        return False
+    # alpha = 0 ignores A and B, even NaN there
+    Abad = A.copy()
+    Abad[0, 0] = np.nan
+    out = _mm(lib, M, N, K, 0.0, Abad, K, B, N, -0.5, C, N)
+    if not np.array_equal(out, (-0.5 * C.astype(np.float64)).astype(np.float32)):
+        return False
+    # alpha = 0 and beta = 0 give zeros
+    if not np.array_equal(_mm(lib, M, N, K, 0.0, Abad, K, B, N, 0.0, Cbad, N),
+                          np.zeros((M, N), np.float32)):
+        return False
+    # K = 0 gives beta * C
+    out = _mm(lib, M, N, 0, 1.0, np.zeros((M, 1), np.float32), 1, np.zeros((1, N), np.float32),
+              N, 2.0, C, N)
+    if not np.array_equal(out, (2.0 * C).astype(np.float32)):
+        return False
+    # alpha = 1, beta = 1: S + C
+    out = _mm(lib, M, N, K, 1.0, A, K, B, N, 1.0, C, N)
+    if not np.array_equal(out, (S + C).astype(np.float32)):
+        return False
+    # a NaN in A does reach the result when alpha != 0 (row 0 only)
+    out = _mm(lib, M, N, K, 1.0, Abad, K, B, N, 0.0, None, N)
+    if not (np.isnan(out[0]).all() and np.isfinite(out[1:]).all()):
+        return False
+    return True
+
+
+def pin_cancellation(lib):
+    # Exactly representable terms whose running sum needs more than 24 bits: the exact
+    # result (1, 3, ...) is what "sum over k, then one rounding" gives; a sum kept in fp32
+    # loses the small terms.
+    big = float(2 ** 24)
+    A = np.array([[big, 1.0, -big], [1.0, big, 3.0]], np.float32)
+    B = np.array([[1.0], [1.0], [1.0]], np.float32)
+    out = _mm(lib, 2, 1, 3, 1.0, A, 3, B, 1, 0.0, None, 1)
+    want = np.array([[1.0], [big + 4.0]], np.float32)
+    return np.array_equal(out, want)
+
+
+def _exact_cell(A, B, C, i, j, alpha, beta):
+    s = sum(Fraction(float(A[i, k])) * Fraction(float(B[k, j])) for k in range(A.shape[1]))
+    v = Fraction(alpha) * s
+    if beta != 0:
+        v += Fraction(beta) * Fraction(float(C[i, j]))
+    return v
+
+
+def _ulp32(x: float) -> float:
+    x = np.float32(abs(x))
+    return float(np.spacing(x)) if x != 0 else float(np.finfo(np.float32).smallest_subnormal)
+
+
+def pin_brute_force(lib):
+    shapes = list(itertools.product([1, 2, 3, 5, 7], [1, 2, 4, 7], [1, 3, 6, 7]))
+    for n, (M, N, K) in enumerate(shapes):
+        A = synth.normal(M, K, 100 + n)
+        B = synth.normal(K, N, 200 + n)
+        C = synth.normal(M, N, 300 + n)
+        alpha, beta = 0.7, -1.3
+        out = _mm(lib, M, N, K, alpha, A, K, B, N, beta, C, N)
+        for i in range(M):
+            for j in range(N):
+                exact = float(_exact_cell(A, B, C, i, j, alpha, beta))
+                if abs(float(out[i, j]) - exact) > _ulp32(exact):
+                    return False
+    return True
+
+
+def pin_leading_dims(lib):
+    M, N, K = 9, 11, 13
+    A = synth.normal(M, K, 31)
+    B = synth.normal(K, N, 32)
+    C = synth.normal(M, N, 33)
+    packed = _mm(lib, M, N, K, 0.7, A, K, B, N, -1.3, C, N)
+    Ap, Bp, Cp = synth.padded(A, K + 3), synth.padded(B, N + 5), synth.padded(C, N + 2)
+    strided = _mm(lib, M, N, K, 0.7, Ap, K + 3, Bp, N + 5, -1.3, Cp, N + 2)
+    return np.array_equal(packed, strided) and np.isfinite(strided).all()
+
+
+def pin_row_subset(lib):
+    M, N, K = 40, 23, 31
+    A = synth.normal(M, K, 41)
+    B = synth.normal(K, N, 42)
+    C = synth.normal(M, N, 43)
+    full = _mm(lib, M, N, K, 0.7, A, K, B, N, -1.3, C, N)
+    rows = [39, 0, 17, 17, 5]
+    sub = _mm(lib, M, N, K, 0.7, A, K, B, N, -1.3, C, N, rows=rows)
+    return np.array_equal(sub, full[rows])
+
+
+PINS = {
+    "identity": pin_identity,
+    "permutation": pin_permutation,
+    "all_ones": pin_all_ones,
+    "small_int": pin_small_int,
+    "alpha_beta": pin_alpha_beta,
+    "brute_force": pin_brute_force,
+    "cancellation": pin_cancellation,
+    "leading_dims": pin_leading_dims,
+    "row_subset": pin_row_subset,
+}
