@@ -1,0 +1,486 @@
+// simt_gemm.cu: FP32 SIMT GEMM kernels for sm_103a, C = alpha * (A . B) + beta * C, row-major.
+//
+// Design (the tiling ladder of the "GEMM scrapbook" re-done for GB300):
+//  * CTA tile BM x BN, k-tile BK = 32, staged in a STAGES-deep shared-memory ring
+//    ("double buffering", generalised). The A and B k-tiles arrive by TMA
+//    (cp.async.bulk.tensor, completion on an mbarrier) when both operands are 16-byte
+//    aligned with leading dimensions that are multiples of 4, otherwise by cp.async with
+//    zero fill. TMA's out-of-bounds fill and cp.async's zero fill supply the zeros of
+//    ragged M, N and K edges, so the compute loop never branches on edges.
+//  * Warp tile 64 x 64 ("warptiling" chapter), thread tile 8 x 16 (the "2D block-tiling"
+//    outer product: per k, a sliver of 8 A values and 16 B values gives 128 multiply-adds).
+//    The multiply-adds are issued as paired fp32 FMAs (__ffma2_rn, two independent FMAs per
+//    instruction), which halves the issue slots the FMA stream needs on Blackwell and leaves
+//    room for the shared-memory loads. Each output cell still accumulates in fp32 with one
+//    rounding per FMA, in ascending k.
+//  * Shared-memory layout without bank conflicts ("bank-conflict dodging"):
+//    - A tile: BM rows of 32 floats (128 B), the 16-byte chunk c of row m stored at chunk
+//      c ^ (m & 7) (the 128-byte TMA swizzle; the cp.async loader writes the same layout).
+//      Thread row tr owns rows tr, tr + 8, ..., tr + 56 of its warp tile, so the 8 rows one
+//      LDS.128 touches sit in 8 different chunk columns.
+//    - B tile: 32 rows of BN floats, unswizzled; the 4 column threads of a warp read 4
+//      adjacent 16-byte chunks (cols 16q + 4tc).
+//    - A values are read as float4 along k (4 k-steps per load), B values as float4 along n
+//      ("float4" chapter: 128-bit loads), no transposed copy of A is needed.
+//  * Epilogue: alpha * acc + beta * C fused, float4 loads and stores where C allows,
+//    C never read when beta == 0.
+#include "ptx.cuh"
+#include "simt_gemm.cuh"
+
+#include <cstring>
+#include <mutex>
+
+namespace sg {
+namespace {
+
+constexpr int BK = 32;
+
+struct KParams {
+    int M, N, K;
+    float alpha, beta;
+    const float *A;
+    const float *B;
+    float *C;
+    long long lda, ldb, ldc;
+    long long sA, sB, sC;
+    int batch;
+    int tiles_m, tiles_n, group_m;
+    int a_vec4, b_vec4, c_vec4;
+};
+
+// Grouped raster order: GROUP_M consecutive tile rows are swept column by column, so CTAs
+// that run at the same time share A row panels and B column panels in L2.
+__device__ __forceinline__ void tile_coords(int pid, int tiles_m, int tiles_n, int group_m,
+                                            int &tm, int &tn) {
+    const int width = group_m * tiles_n;
+    const int group = pid / width;
+    const int first_m = group * group_m;
+    const int gsize = min(tiles_m - first_m, group_m);
+    const int in = pid - group * width;
+    tm = first_m + in % gsize;
+    tn = in / gsize;
+}
+
+// One k-tile (32 k-steps) of outer products for one thread's 8 x 16 tile.
+//   a_base: sA + (wm0 + tr) * 32, row r of the thread tile is 8 * r rows further (256 floats).
+//   b_base: sB + wn0 + 4 * tc, chunk q of the thread tile is 16 * q floats further.
+template <int BN>
+__device__ __forceinline__ void compute_ktile(const float *__restrict__ a_base, int tr,
+                                              const float *__restrict__ b_base,
+                                              float2 (&acc)[8][8]) {
+#pragma unroll
+    for (int kg = 0; kg < BK / 4; ++kg) {
+        float4 a[8];
+        const int achunk = (kg ^ tr) << 2;
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+            a[r] = *reinterpret_cast<const float4 *>(a_base + r * 256 + achunk);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            float4 b[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                b[q] = *reinterpret_cast<const float4 *>(b_base + (kg * 4 + kk) * BN + 16 * q);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float av = kk == 0 ? a[r].x : kk == 1 ? a[r].y : kk == 2 ? a[r].z : a[r].w;
+                const float2 a2 = make_float2(av, av);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[r][2 * q] = __ffma2_rn(a2, make_float2(b[q].x, b[q].y), acc[r][2 * q]);
+                    acc[r][2 * q + 1] =
+                        __ffma2_rn(a2, make_float2(b[q].z, b[q].w), acc[r][2 * q + 1]);
+                }
+            }
+        }
+    }
+}
+
+// cp.async fill of one stage: A tile (BM x 32, swizzled rows) and B tile (32 x BN).
+template <int BM, int BN, int THREADS>
+__device__ __forceinline__ void cp_async_stage(float *sA, float *sB, const KParams &p,
+                                               const float *Ab, const float *Bb, int m0, int n0,
+                                               int k0, int tid) {
+    if (p.a_vec4) {
+#pragma unroll 4
+        for (int c = tid; c < BM * (BK / 4); c += THREADS) {
+            const int m = c >> 3, kc = c & 7;
+            const int gm = m0 + m, gk = k0 + kc * 4;
+            uint32_t bytes = 0;
+            const float *src = Ab;
+            if (gm < p.M && gk < p.K) {
+                bytes = static_cast<uint32_t>(min(4, p.K - gk)) * 4u;
+                src = Ab + static_cast<long long>(gm) * p.lda + gk;
+            }
+            cp_async_16(smem_addr(sA + m * BK + ((kc ^ (m & 7)) << 2)), src, bytes);
+        }
+    } else {
+#pragma unroll 4
+        for (int e = tid; e < BM * BK; e += THREADS) {
+            const int m = e >> 5, k = e & 31;
+            const int gm = m0 + m, gk = k0 + k;
+            uint32_t bytes = 0;
+            const float *src = Ab;
+            if (gm < p.M && gk < p.K) {
+                bytes = 4u;
+                src = Ab + static_cast<long long>(gm) * p.lda + gk;
+            }
+            cp_async_4(smem_addr(sA + m * BK + (((k >> 2) ^ (m & 7)) << 2) + (k & 3)), src, bytes);
+        }
+    }
+    if (p.b_vec4) {
+#pragma unroll 4
+        for (int c = tid; c < BK * (BN / 4); c += THREADS) {
+            const int k = c / (BN / 4), nc = c % (BN / 4);
+            const int gk = k0 + k, gn = n0 + nc * 4;
+            uint32_t bytes = 0;
+            const float *src = Bb;
+            if (gk < p.K && gn < p.N) {
+                bytes = static_cast<uint32_t>(min(4, p.N - gn)) * 4u;
+                src = Bb + static_cast<long long>(gk) * p.ldb + gn;
+            }
+            cp_async_16(smem_addr(sB + k * BN + nc * 4), src, bytes);
+        }
+    } else {
+#pragma unroll 4
+        for (int e = tid; e < BK * BN; e += THREADS) {
+            const int k = e / BN, n = e % BN;
+            const int gk = k0 + k, gn = n0 + n;
+            uint32_t bytes = 0;
+            const float *src = Bb;
+            if (gk < p.K && gn < p.N) {
+                bytes = 4u;
+                src = Bb + static_cast<long long>(gk) * p.ldb + gn;
+            }
+            cp_async_4(smem_addr(sB + k * BN + n), src, bytes);
+        }
+    }
+}
+
+// alpha * acc + beta * C for the thread's 8 x 16 cells (rows tr + 8r, cols 16q + 4tc + e).
+__device__ __forceinline__ void epilogue(const KParams &p, float *Cb, int row0, int col0,
+                                         const float2 (&acc)[8][8]) {
+    const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int gm = row0 + 8 * r;
+        if (gm >= p.M) continue;
+        float *crow = Cb + static_cast<long long>(gm) * p.ldc;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int gn = col0 + 16 * q;
+            const float v[4] = {acc[r][2 * q].x, acc[r][2 * q].y, acc[r][2 * q + 1].x,
+                                acc[r][2 * q + 1].y};
+            if (p.c_vec4 && gn + 3 < p.N) {
+                float4 o;
+                if (beta != 0.0f) {
+                    const float4 c = *reinterpret_cast<const float4 *>(crow + gn);
+                    o = make_float4(fmaf(alpha, v[0], beta * c.x), fmaf(alpha, v[1], beta * c.y),
+                                    fmaf(alpha, v[2], beta * c.z), fmaf(alpha, v[3], beta * c.w));
+                } else {
+                    o = make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
+                }
+                *reinterpret_cast<float4 *>(crow + gn) = o;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (gn + e < p.N) {
+                        crow[gn + e] = beta != 0.0f ? fmaf(alpha, v[e], beta * crow[gn + e])
+                                                    : alpha * v[e];
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int LOADER>
+__global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, 1)
+    simt_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
+                     const __grid_constant__ CUtensorMap mapB, const KParams p) {
+    constexpr int THREADS = WARPS_M * WARPS_N * 32;
+    static_assert(BM == WARPS_M * 64 && BN == WARPS_N * 64, "64 x 64 warp tiles");
+    constexpr int A_FLOATS = BM * BK;
+    constexpr int STAGE_FLOATS = A_FLOATS + BK * BN;
+    constexpr uint32_t STAGE_BYTES = STAGE_FLOATS * 4;
+
+    extern __shared__ uint8_t smem_raw[];
+    // The 128-byte swizzle pattern repeats every 1024 bytes of shared address space.
+    const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+    float *smem = reinterpret_cast<float *>(smem_raw + pad);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_FLOATS);
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int wm0 = (warp / WARPS_N) * 64, wn0 = (warp % WARPS_N) * 64;
+    const int tr = lane >> 2, tc = lane & 3;
+
+    int tm, tn;
+    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    const int m0 = tm * BM, n0 = tn * BN;
+    const int KT = (p.K + BK - 1) / BK;
+
+    if (tid == 0) {
+        s_abort = 0;
+        if (LOADER == kLoaderTma) {
+            tma_prefetch_desc(&mapA);
+            tma_prefetch_desc(&mapB);
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+            mbar_init_fence();
+        }
+    }
+    __syncthreads();
+
+    int issued = 0, consumed = 0;  // TMA k-tiles over the whole batch loop (ring position)
+    for (int b = blockIdx.y; b < p.batch; b += gridDim.y) {
+        float2 acc[8][8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
+
+        if (LOADER == kLoaderTma) {
+            auto issue = [&](int kt) {
+                const int s = issued % STAGES;
+                float *sA = smem + s * STAGE_FLOATS;
+                mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                tma_load_3d(sA, &mapA, &full[s], kt * BK, m0, b);
+                tma_load_3d(sA + A_FLOATS, &mapB, &full[s], n0, kt * BK, b);
+                ++issued;
+            };
+            if (tid == 0)
+                for (int kt = 0; kt < STAGES && kt < KT; ++kt) issue(kt);
+            else
+                issued += min(STAGES, KT);
+            for (int kt = 0; kt < KT; ++kt) {
+                const int s = consumed % STAGES;
+                if (!mbar_wait(&full[s], (consumed / STAGES) & 1)) s_abort = 1;
+                const float *sA = smem + s * STAGE_FLOATS;
+                compute_ktile<BN>(sA + (wm0 + tr) * BK, tr, sA + A_FLOATS + wn0 + 4 * tc, acc);
+                ++consumed;
+                __syncthreads();  // every warp is done reading stage s
+                if (s_abort) break;
+                if (kt + STAGES < KT) {
+                    if (tid == 0)
+                        issue(kt + STAGES);
+                    else
+                        ++issued;
+                }
+            }
+        } else {
+            const float *Ab = p.A + static_cast<long long>(b) * p.sA;
+            const float *Bb = p.B + static_cast<long long>(b) * p.sB;
+#pragma unroll
+            for (int s = 0; s < STAGES - 1; ++s) {
+                if (s < KT) {
+                    float *sA = smem + s * STAGE_FLOATS;
+                    cp_async_stage<BM, BN, THREADS>(sA, sA + A_FLOATS, p, Ab, Bb, m0, n0, s * BK,
+                                                    tid);
+                }
+                cp_async_commit();
+            }
+            for (int kt = 0; kt < KT; ++kt) {
+                cp_async_wait<STAGES - 2>();
+                __syncthreads();  // stage kt landed for all threads; stage kt - 1 is free
+                const int nk = kt + STAGES - 1;
+                if (nk < KT) {
+                    float *sN = smem + (nk % STAGES) * STAGE_FLOATS;
+                    cp_async_stage<BM, BN, THREADS>(sN, sN + A_FLOATS, p, Ab, Bb, m0, n0,
+                                                    nk * BK, tid);
+                }
+                cp_async_commit();
+                const float *sA = smem + (kt % STAGES) * STAGE_FLOATS;
+                compute_ktile<BN>(sA + (wm0 + tr) * BK, tr, sA + A_FLOATS + wn0 + 4 * tc, acc);
+            }
+            cp_async_wait<0>();
+            __syncthreads();
+        }
+        if (s_abort) break;
+        epilogue(p, p.C + static_cast<long long>(b) * p.sC, m0 + wm0 + tr, n0 + wn0 + 4 * tc, acc);
+    }
+
+    if (LOADER == kLoaderTma && s_abort && tid == 0) {
+        // Let copies already in flight land before the CTA's shared memory is released.
+        for (; consumed < issued; ++consumed)
+            if (!mbar_wait(&full[consumed % STAGES], (consumed / STAGES) & 1)) break;
+    }
+}
+
+// ---- host side ---------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+long long round_up16(long long v) { return (v + 15) / 16 * 16; }
+
+// rows x cols fp32 matrix with leading dimension ld, `batch` copies `stride` elements apart,
+// read in boxes of box_rows x box_cols.
+bool make_map(CUtensorMap *map, const float *base, long long rows, long long cols, long long ld,
+              long long stride, int batch, int box_rows, int box_cols, bool swizzle128) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const long long stride_bytes =
+        batch > 1 ? stride * 4 : round_up16(rows * ld * 4 > 16 ? rows * ld * 4 : 16);
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 4),
+                             static_cast<cuuint64_t>(stride_bytes)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+bool operand_vec4(const float *ptr, long long ld, long long stride, int batch) {
+    return aligned16(ptr) && ld % 4 == 0 && (batch <= 1 || stride % 4 == 0);
+}
+
+bool tma_ok(const SimtProblem &p) {
+    // TMA needs 16-byte aligned bases and byte strides; a zero batch stride (broadcast
+    // operand) goes to the cp.async loader.
+    if (!operand_vec4(p.A, p.lda, p.strideA, p.batch)) return false;
+    if (!operand_vec4(p.B, p.ldb, p.strideB, p.batch)) return false;
+    if (p.batch > 1 && (p.strideA == 0 || p.strideB == 0)) return false;
+    return true;
+}
+
+const SimtConfig kConfigs[] = {
+    {"dp_tma_128x256_s4", 128, 256, 2, 4, 4, kLoaderTma, kScheduleDataParallel},
+    {"dp_tma_256x128_s4", 256, 128, 4, 2, 4, kLoaderTma, kScheduleDataParallel},
+    {"dp_tma_128x128_s3", 128, 128, 2, 2, 3, kLoaderTma, kScheduleDataParallel},
+    {"dp_cpasync_128x256_s4", 128, 256, 2, 4, 4, kLoaderCpAsync, kScheduleDataParallel},
+    {"dp_cpasync_128x128_s3", 128, 128, 2, 2, 3, kLoaderCpAsync, kScheduleDataParallel},
+};
+constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
+
+constexpr int kMaxDevices = 64;
+
+template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int LOADER>
+cudaError_t launch_impl(int id, const SimtProblem &p, cudaStream_t stream, const char **detail) {
+    constexpr int THREADS = WARPS_M * WARPS_N * 32;
+    constexpr size_t SMEM = static_cast<size_t>(STAGES) * (BM * BK + BK * BN) * 4 +
+                            STAGES * sizeof(uint64_t) + 1024;
+    auto kernel = simt_gemm_kernel<BM, BN, WARPS_M, WARPS_N, STAGES, LOADER>;
+
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) {
+        *detail = "cudaGetDevice failed";
+        return err;
+    }
+    static std::once_flag attr_once[kMaxDevices];
+    static cudaError_t attr_err[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) {
+        *detail = "device ordinal above the library's limit";
+        return cudaErrorInvalidDevice;
+    }
+    std::call_once(attr_once[dev], [&] {
+        attr_err[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(SMEM));
+    });
+    if (attr_err[dev] != cudaSuccess) {
+        *detail = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+        return attr_err[dev];
+    }
+
+    KParams kp;
+    kp.M = p.M;
+    kp.N = p.N;
+    kp.K = p.K;
+    kp.alpha = p.alpha;
+    kp.beta = p.beta;
+    kp.A = p.A;
+    kp.B = p.B;
+    kp.C = p.C;
+    kp.lda = p.lda;
+    kp.ldb = p.ldb;
+    kp.ldc = p.ldc;
+    kp.sA = p.strideA;
+    kp.sB = p.strideB;
+    kp.sC = p.strideC;
+    kp.batch = p.batch;
+    kp.tiles_m = (p.M + BM - 1) / BM;
+    kp.tiles_n = (p.N + BN - 1) / BN;
+    kp.group_m = 8;
+    kp.a_vec4 = operand_vec4(p.A, p.lda, p.strideA, p.batch);
+    kp.b_vec4 = operand_vec4(p.B, p.ldb, p.strideB, p.batch);
+    kp.c_vec4 = operand_vec4(p.C, p.ldc, p.strideC, p.batch);
+
+    CUtensorMap mapA, mapB;
+    memset(&mapA, 0, sizeof(mapA));
+    memset(&mapB, 0, sizeof(mapB));
+    if (LOADER == kLoaderTma) {
+        if (!make_map(&mapA, p.A, p.M, p.K, p.lda, p.strideA, p.batch, BM, BK, true) ||
+            !make_map(&mapB, p.B, p.K, p.N, p.ldb, p.strideB, p.batch, BK, BN, false)) {
+            *detail = "cuTensorMapEncodeTiled rejected an operand";
+            return cudaErrorInvalidValue;
+        }
+    }
+    const long long tiles = static_cast<long long>(kp.tiles_m) * kp.tiles_n;
+    dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.batch < 65535 ? p.batch : 65535));
+    kernel<<<grid, THREADS, SMEM, stream>>>(mapA, mapB, kp);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) *detail = "kernel launch failed";
+    (void)id;
+    return err;
+}
+
+}  // namespace
+
+int simt_num_configs() { return kNumConfigs; }
+
+const SimtConfig &simt_config(int id) { return kConfigs[id]; }
+
+bool simt_config_supports(int id, const SimtProblem &p) {
+    if (id < 0 || id >= kNumConfigs) return false;
+    if (kConfigs[id].loader == kLoaderTma) return tma_ok(p);
+    return true;
+}
+
+cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const char **detail) {
+    switch (id) {
+        case 0: return launch_impl<128, 256, 2, 4, 4, kLoaderTma>(id, p, stream, detail);
+        case 1: return launch_impl<256, 128, 4, 2, 4, kLoaderTma>(id, p, stream, detail);
+        case 2: return launch_impl<128, 128, 2, 2, 3, kLoaderTma>(id, p, stream, detail);
+        case 3: return launch_impl<128, 256, 2, 4, 4, kLoaderCpAsync>(id, p, stream, detail);
+        case 4: return launch_impl<128, 128, 2, 2, 3, kLoaderCpAsync>(id, p, stream, detail);
+        default: *detail = "unknown SIMT configuration"; return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t release_workspaces() { return cudaSuccess; }
+
+unsigned int simt_take_fault_word(cudaStream_t stream) {
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbolAsync(&word, g_fault_word, sizeof(word), 0, cudaMemcpyDeviceToHost,
+                                  stream) != cudaSuccess)
+        return 0;
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbolAsync(g_fault_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+    cudaStreamSynchronize(stream);
+    return word;
+}
+
+}  // namespace sg

@@ -1,0 +1,59 @@
+// simt_gemm.cuh: host-visible description of the FP32 SIMT kernels (tile configurations and
+// the launch entry used by the dispatcher in sgemm_api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sg {
+
+// How A and B tiles travel from global to shared memory.
+enum LoaderKind : int {
+    kLoaderTma = 0,      // cp.async.bulk.tensor (TMA), 16-byte aligned operands only
+    kLoaderCpAsync = 1,  // cp.async, 16-byte chunks where an operand allows, else 4-byte
+};
+
+// Order in which tiles are assigned to CTAs.
+enum ScheduleKind : int {
+    kScheduleDataParallel = 0,  // one CTA per output tile (grouped raster order)
+    kScheduleStreamK = 1,       // persistent CTAs, last partial wave split along K
+};
+
+struct SimtConfig {
+    const char *name;
+    int bm, bn;      // CTA tile
+    int warps_m, warps_n;
+    int stages;      // depth of the shared-memory ring
+    int loader;      // LoaderKind
+    int schedule;    // ScheduleKind
+};
+
+// One problem (or one batch of equally shaped problems) as the kernels see it.
+struct SimtProblem {
+    int M, N, K;
+    float alpha, beta;
+    const float *A;
+    const float *B;
+    float *C;
+    long long lda, ldb, ldc;
+    long long strideA, strideB, strideC;  // element strides between batch entries
+    int batch;
+};
+
+int simt_num_configs();
+const SimtConfig &simt_config(int id);
+
+// True when config `id` can run this problem (alignment needs of its loader).
+bool simt_config_supports(int id, const SimtProblem &p);
+
+// Launches config `id` on `stream`. Returns cudaSuccess or the launch / setup error;
+// `detail` receives a static description of a failing step.
+cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const char **detail);
+
+// Reads and clears this file's device fault word on the current device.
+unsigned int simt_take_fault_word(cudaStream_t stream);
+
+// Frees every per-device workspace the SIMT kernels allocated (stream-K partial tiles).
+cudaError_t release_workspaces();
+
+}  // namespace sg

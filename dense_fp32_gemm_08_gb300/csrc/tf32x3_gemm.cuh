@@ -1,0 +1,18 @@
+// tf32x3_gemm.cuh: the tcgen05 tensor-core path that emulates fp32 with three TF32 products.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "simt_gemm.cuh"
+
+namespace sg {
+
+// True when the 3xTF32 kernel can run this problem (16-byte aligned A and B, leading
+// dimensions and batch strides multiples of 4 elements).
+bool tf32x3_supports(const SimtProblem &p);
+
+cudaError_t tf32x3_launch(const SimtProblem &p, cudaStream_t stream, const char **detail);
+
+unsigned int tf32x3_take_fault_word(cudaStream_t stream);
+
+}  // namespace sg

@@ -1,0 +1,153 @@
+/*
+ * sgemm.h: C ABI of the GB300 (sm_103a) single-precision GEMM library.
+ *
+ * Operation, for every entry point below:
+ *
+ *     C = alpha * (A . B) + beta * C
+ *
+ * with A an M x K, B a K x N and C an M x N matrix of fp32 values, all row-major: element
+ * (r, c) of a matrix with leading dimension ld sits at index r * ld + c. This is the SGEMM of
+ * "a CUDA matmul" (section 00, and the naive kernel of section 02, whose strides are the
+ * packed lda = K, ldb = N, ldc = N generalised here), and the GEMM definition of the "GEMM
+ * scrapbook" (each cell of C is one row of A dotted with one column of B).
+ *
+ * Conventions shared by all entry points
+ * --------------------------------------
+ * Memory and ownership: A, B and C are device pointers owned by the caller (for example
+ *   torch CUDA tensors). The library keeps no reference to them after the call returns.
+ *   No entry point allocates device memory per call. The stream-K split of the tile grid
+ *   uses one workspace per device, allocated on first use and kept until
+ *   sgemm_release_workspace().
+ * Streams: every compute call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *   legacy default stream) and does not synchronise. Results are visible to later work on
+ *   the same stream.
+ * alpha and beta (BLAS convention): beta == 0 means C is write-only (NaN or Inf already in
+ *   C does not reach the result). alpha == 0 or K == 0 means C = beta * C, and A and B are
+ *   not read (they may then be NULL).
+ * Degenerate sizes: M == 0, N == 0 or batch == 0 is a no-op that returns SGEMM_OK without
+ *   touching any pointer.
+ * Alignment: none is required. 16-byte aligned pointers with leading dimensions (and batch
+ *   strides) that are multiples of 4 elements select the TMA fast path; anything else runs a
+ *   cp.async path with the same arithmetic.
+ * Aliasing: C must not overlap A or B (undefined result, as in BLAS).
+ * Accuracy: the SIMT entry points accumulate in fp32 with fused multiply-adds in ascending k
+ *   for every output cell; the result differs from the exact value by rounding only.
+ * Errors: argument errors return SGEMM_ERR_INVALID_VALUE before any device work is queued.
+ *   A failed launch returns SGEMM_ERR_LAUNCH. Every wait inside a kernel is bounded; a wait
+ *   that expires sets a device error word, makes the kernel return early (its output is then
+ *   undefined) and is reported as SGEMM_ERR_TIMEOUT by sgemm_device_status(). A readable
+ *   message for the calling thread's last non-OK return is given by sgemm_last_error().
+ * Thread safety: calls from several host threads are safe; each thread has its own
+ *   sgemm_last_error() text.
+ */
+#ifndef DENSE_FP32_GEMM_08_GB300_SGEMM_H
+#define DENSE_FP32_GEMM_08_GB300_SGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sgemm_status {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_VALUE = 1, /* bad size, leading dimension, stride or NULL pointer */
+    SGEMM_ERR_LAUNCH = 2,        /* the CUDA runtime refused a launch or a setup call */
+    SGEMM_ERR_TIMEOUT = 3,       /* a bounded wait inside a kernel expired */
+    SGEMM_ERR_UNSUPPORTED = 4    /* valid arguments this build cannot run (e.g. no GPU) */
+} sgemm_status_t;
+
+/*
+ * C = alpha * (A . B) + beta * C on the FP32 SIMT path ("GEMM scrapbook": 2D block tiling
+ * with register outer products, float4 loads, warp tiling and double buffering; here a
+ * multi-stage TMA or cp.async shared-memory ring and paired fp32 FMAs).
+ *   M, N, K   >= 0.
+ *   A         M x K, lda >= max(1, K).   B   K x N, ldb >= max(1, N).
+ *   C         M x N, ldc >= max(1, N).
+ *   A, B may be NULL only when alpha == 0 or K == 0; C may be NULL only when M or N is 0.
+ *   stream    cudaStream_t or NULL.
+ */
+sgemm_status_t sgemm(int64_t M, int64_t N, int64_t K, float alpha,
+                     const float *A, int64_t lda, const float *B, int64_t ldb,
+                     float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * `batch` independent products: problem b uses A + b * strideA, B + b * strideB and
+ * C + b * strideC (element strides), each with the sizes and leading dimensions above.
+ *   batch >= 0; strideA, strideB >= 0 (0 broadcasts one operand); strideC >= M * ldc when
+ *   batch > 1 (the C matrices of different problems must not overlap).
+ */
+sgemm_status_t sgemm_strided_batched(int64_t M, int64_t N, int64_t K, float alpha,
+                                     const float *A, int64_t lda, int64_t strideA,
+                                     const float *B, int64_t ldb, int64_t strideB,
+                                     float beta, float *C, int64_t ldc, int64_t strideC,
+                                     int64_t batch, void *stream);
+
+/*
+ * The same operation on the tensor cores (tcgen05 MMA, accumulator in tensor memory),
+ * emulating fp32 with three TF32 products. Each operand value x is split as
+ * x = big + small with big = tf32_rna(x) and small = tf32_rna(x - big); the accumulator
+ * receives big_A.big_B + big_A.small_B + small_A.big_B. The pages name tensor cores (TF32
+ * at twice the FP32 rate) only as "a different vehicle" ("GEMM scrapbook", closing
+ * remarks); the three-product split itself is not on the pages. Same arguments, errors and
+ * conventions as sgemm(); it needs A, B 16-byte aligned with lda, ldb multiples of 4, and
+ * returns SGEMM_ERR_UNSUPPORTED otherwise.
+ */
+sgemm_status_t sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha,
+                            const float *A, int64_t lda, const float *B, int64_t ldb,
+                            float beta, float *C, int64_t ldc, void *stream);
+
+/* Batched form of sgemm_3xtf32; the arguments are those of sgemm_strided_batched. */
+sgemm_status_t sgemm_3xtf32_strided_batched(int64_t M, int64_t N, int64_t K, float alpha,
+                                            const float *A, int64_t lda, int64_t strideA,
+                                            const float *B, int64_t ldb, int64_t strideB,
+                                            float beta, float *C, int64_t ldc,
+                                            int64_t strideC, int64_t batch, void *stream);
+
+/* Static text for a status code (never NULL). */
+const char *sgemm_status_string(sgemm_status_t status);
+
+/* Detail message for the calling thread's most recent non-OK return ("" if none). */
+const char *sgemm_last_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the current device.
+ * Returns SGEMM_ERR_TIMEOUT if a kernel's bounded wait expired since the previous call,
+ * SGEMM_ERR_LAUNCH if the stream reports a CUDA error, SGEMM_OK otherwise.
+ */
+sgemm_status_t sgemm_device_status(void *stream);
+
+/* Frees the per-device stream-K workspaces (the next call that needs one allocates it
+ * again). Synchronises the device first. */
+sgemm_status_t sgemm_release_workspace(void);
+
+/*
+ * Kernel configurations (tile shape, pipeline depth, loader, tile schedule) of the SIMT
+ * path. sgemm_num_configs() is the table size; sgemm_config_name(i) a static name
+ * (NULL when i is out of range).
+ */
+int sgemm_num_configs(void);
+const char *sgemm_config_name(int id);
+
+/*
+ * The configuration the dispatcher picks for these arguments (the id in the table above),
+ * or -1 when no kernel would run (degenerate sizes, alpha == 0, K == 0, invalid arguments).
+ * Reads no device memory.
+ */
+int sgemm_select_config(int64_t M, int64_t N, int64_t K, float alpha,
+                        const float *A, int64_t lda, const float *B, int64_t ldb,
+                        const float *C, int64_t ldc, int64_t batch);
+
+/*
+ * Forces configuration `id` for subsequent SIMT calls from every thread (-1 restores the
+ * per-shape table). A forced configuration that cannot run an operand's alignment falls
+ * back to the table's choice. Returns SGEMM_ERR_INVALID_VALUE for an unknown id.
+ * The environment variable SGEMM_FORCE_CONFIG=<id> sets the same at load time.
+ */
+sgemm_status_t sgemm_force_config(int id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_FP32_GEMM_08_GB300_SGEMM_H */
