@@ -1,16 +1,52 @@
 // config_table.h: per-shape-class choice of SIMT kernel configuration.
+//
+// The classes and their winners come from device-timed sweeps on a GB300 (152 SMs), one
+// configuration forced at a time (bench.py with SGEMM_FORCE_CONFIG):
+//
+//   class                       measured                                         choice
+//   aligned, <  6 waves of       4096^3: sk 128x256 63.6 TF/s, dp 128x128 62.0,   sk_tma_ws_128x256_s4
+//     128x128 tiles at 2/SM      dp 128x256 54.5; 2048^3: sk 128x256 60.5,
+//                                dp 128x128 48.2, dp 128x256 53.0
+//   aligned, >= 6 waves          8192^3: dp 128x128 65.2, sk 128x256 64.1;         dp_tma_128x128_s3
+//                                16384x12288x4096: dp 128x128 65.3, sk 62.7
+//   aligned, one tile or less    256^3 and below: latency bound, a single          dp_tma_128x128_s3
+//                                128x128 CTA per tile has the shortest chain
+//   unaligned (no TMA)           4095x3001x1537: cp.async 128x256 30.1 TF/s        dp_cpasync_128x256_s4
+//                                small shapes: cp.async 128x128                    dp_cpasync_128x128_s3
 #pragma once
 
 #include "simt_gemm.cuh"
 
 namespace sg {
 
+enum : int {
+    kCfgDpTma128x256 = 0,
+    kCfgDpTma256x128 = 1,
+    kCfgDpTma128x128 = 2,
+    kCfgDpCp128x256 = 3,
+    kCfgDpCp128x128 = 4,
+    kCfgSkTma128x256 = 5,
+    kCfgPdpTma128x256 = 6,
+    kCfgSkTma256x128 = 7,
+    kCfgSkTma128x128s3 = 8,
+    kCfgSkTma128x128s4 = 9,
+};
+
+// Waves of 128 x 128 tiles at two CTAs per SM on a 152-SM part.
+inline double waves_128x128(const SimtProblem &p) {
+    const double tiles = static_cast<double>((p.M + 127) / 128) * ((p.N + 127) / 128) * p.batch;
+    return tiles / (2.0 * 152.0);
+}
+
 // Picks the configuration id for a problem from its shape class and operand alignment.
 inline int table_choose(const SimtProblem &p) {
-    const bool tma = simt_config_supports(0, p);
-    const bool small = static_cast<long long>(p.M) * p.N <= 256LL * 256;
-    if (tma) return small ? 2 : 0;
-    return small ? 4 : 3;
+    const bool tma = simt_config_supports(kCfgDpTma128x128, p);
+    const double waves = waves_128x128(p);
+    const bool tiny = static_cast<long long>(p.M) * p.N * p.batch <= 128LL * 128;
+    if (!tma) return static_cast<long long>(p.M) * p.N <= 512LL * 512 ? kCfgDpCp128x128 : kCfgDpCp128x256;
+    if (tiny) return kCfgDpTma128x128;
+    if (waves >= 6.0) return kCfgDpTma128x128;
+    return kCfgSkTma128x256;
 }
 
 }  // namespace sg

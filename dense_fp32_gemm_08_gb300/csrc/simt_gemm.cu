@@ -27,8 +27,11 @@
 #include "ptx.cuh"
 #include "simt_gemm.cuh"
 
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 namespace sg {
 namespace {
@@ -307,6 +310,264 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, 1)
     }
 }
 
+// ---- persistent kernel with a stream-K tail -------------------------------------------------
+//
+// Thread 0 issues the TMA loads of every k-tile the CTA will consume across all of its output
+// tiles, STAGES - 1 k-tiles ahead of the compute (the ring does not drain between tiles).
+// The grid is persistent (as many CTAs as fit on the SMs at once). Output tiles
+// [0, dp_tiles) are dealt round-robin whole; the remaining tiles' k-iterations are split into
+// one contiguous range per CTA (stream-K), so every CTA does the same number of k-iterations
+// and no partial wave is left idle.
+//
+// A tile cut by a range boundary is finished by the CTA whose range holds the tile's last
+// k-iteration (its "owner"); every other CTA that worked on the tile stores its fp32 partial
+// sums in its own workspace slot and publishes them with a per-warp flag (release / acquire,
+// value = this launch's epoch). Each CTA walks its own range backwards, so the pieces it hands
+// to a higher-numbered owner are computed first and the piece it owns (whose contributors
+// are lower-numbered CTAs) last: owners wait only on lower-numbered CTAs, which are resident
+// or finished. Thread t of an owner warp reads exactly the partials thread t of the same warp
+// of the contributing CTA wrote, so no cross-warp synchronisation is needed. The sum over
+// pieces runs in a fixed order: results are deterministic.
+
+struct PParams {
+    KParams k;
+    int KT;               // k-tiles per output tile
+    int tiles_per_batch;  // tiles_m * tiles_n
+    int dp_tiles;         // tiles done whole in the data-parallel phase
+    int G;                // CTAs in the persistent grid
+    long long sk_base;    // stream-K k-iterations per CTA (the first sk_rem CTAs do one more)
+    int sk_rem;
+    float4 *ws;           // partial sums: [G][consumer warps][32][32] float4
+    unsigned int *flags;  // [G][consumer warps]
+    unsigned int epoch;   // this launch's flag value (never 0)
+};
+
+struct Segment {
+    int tile, k0, k1;
+};
+
+// The ordered list of segments (tile, k-range) CTA `c` processes: its data-parallel tiles,
+// then its stream-K range from the last tile backwards.
+struct SegmentWalker {
+    int t, dp_tiles, G, KT;
+    long long s, cur_end;
+
+    __device__ SegmentWalker(const PParams &p, int c) {
+        t = c;
+        dp_tiles = p.dp_tiles;
+        G = p.G;
+        KT = p.KT;
+        const long long base = static_cast<long long>(p.dp_tiles) * p.KT;
+        s = base + c * p.sk_base + min(c, p.sk_rem);
+        cur_end = s + p.sk_base + (c < p.sk_rem ? 1 : 0);
+    }
+
+    __device__ bool next(Segment &seg) {
+        if (t < dp_tiles) {
+            seg.tile = t;
+            seg.k0 = 0;
+            seg.k1 = KT;
+            t += G;
+            return true;
+        }
+        if (cur_end <= s) return false;
+        const long long tile = (cur_end - 1) / KT;
+        const long long tb = tile * KT;
+        const long long lo = s > tb ? s : tb;
+        seg.tile = static_cast<int>(tile);
+        seg.k0 = static_cast<int>(lo - tb);
+        seg.k1 = static_cast<int>(cur_end - tb);
+        cur_end = lo;
+        return true;
+    }
+};
+
+__device__ __forceinline__ long long sk_start(const PParams &p, int c) {
+    return static_cast<long long>(p.dp_tiles) * p.KT + c * p.sk_base + min(c, p.sk_rem);
+}
+
+__device__ __forceinline__ void tile_origin(const PParams &p, int tile, int BM_, int BN_, int &b,
+                                            int &m0, int &n0) {
+    b = tile / p.tiles_per_batch;
+    int tm, tn;
+    tile_coords(tile - b * p.tiles_per_batch, p.k.tiles_m, p.k.tiles_n, p.k.group_m, tm, tn);
+    m0 = tm * BM_;
+    n0 = tn * BN_;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned int *p, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Spins (bounded by kWaitLimitNs) until *flag == value. Returns false on timeout.
+__device__ __forceinline__ bool wait_flag(const unsigned int *flag, unsigned int value) {
+    if (ld_acquire_gpu(flag) == value) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (ld_acquire_gpu(flag) == value) return true;
+        if ((spin & 15u) == 0u) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                raise_fault(kFaultTimeout);
+                return false;
+            }
+            __nanosleep(64);
+        }
+    }
+}
+
+// Streams the k-tiles of a CTA's segment list into the shared-memory ring (thread 0 only).
+struct TmaProducer {
+    SegmentWalker walk;
+    Segment seg;
+    int kt, b, m0, n0;
+    bool live;
+
+    __device__ TmaProducer(const PParams &p, int c) : walk(p, c), kt(0), b(0), m0(0), n0(0) {
+        live = walk.next(seg);
+        kt = seg.k0;
+    }
+
+    template <int BM, int BN>
+    __device__ bool next(const PParams &p) {
+        while (live && kt >= seg.k1) {
+            live = walk.next(seg);
+            kt = seg.k0;
+        }
+        if (!live) return false;
+        if (kt == seg.k0) tile_origin(p, seg.tile, BM, BN, b, m0, n0);
+        return true;
+    }
+};
+
+// MAXREG caps registers per thread: four-warp tiles run two CTAs per SM and must leave room
+// for both in the register file.
+template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG>
+__global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
+    simt_gemm_persistent_kernel(const __grid_constant__ CUtensorMap mapA,
+                                const __grid_constant__ CUtensorMap mapB, const PParams p) {
+    constexpr int WARPS = WARPS_M * WARPS_N;
+    static_assert(BM == WARPS_M * 64 && BN == WARPS_N * 64, "64 x 64 warp tiles");
+    static_assert(STAGES >= 2, "at least double buffering");
+    constexpr int A_FLOATS = BM * BK;
+    constexpr int STAGE_FLOATS = A_FLOATS + BK * BN;
+    constexpr uint32_t STAGE_BYTES = STAGE_FLOATS * 4;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+    float *smem = reinterpret_cast<float *>(smem_raw + pad);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_FLOATS);
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cta = blockIdx.x;
+
+    if (tid == 0) {
+        s_abort = 0;
+        tma_prefetch_desc(&mapA);
+        tma_prefetch_desc(&mapB);
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    // Thread 0 streams the k-tiles of the CTA's whole segment list into the ring: the first
+    // STAGES up front, then one refill into the stage just released after every k-tile.
+    TmaProducer prod(p, cta);
+    int issued = 0;
+    auto produce = [&]() {
+        const int s = issued % STAGES;
+        float *sA = smem + s * STAGE_FLOATS;
+        mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+        tma_load_3d(sA, &mapA, &full[s], prod.kt * BK, prod.m0, prod.b);
+        tma_load_3d(sA + A_FLOATS, &mapB, &full[s], prod.n0, prod.kt * BK, prod.b);
+        ++prod.kt;
+        ++issued;
+    };
+    if (tid == 0)
+        while (issued < STAGES && prod.template next<BM, BN>(p)) produce();
+
+    const int wm0 = (warp / WARPS_N) * 64, wn0 = (warp % WARPS_N) * 64;
+    const int tr = lane >> 2, tc = lane & 3;
+    SegmentWalker walk(p, cta);
+    Segment seg;
+    int i = 0;
+    while (walk.next(seg)) {
+        int b, m0, n0;
+        tile_origin(p, seg.tile, BM, BN, b, m0, n0);
+        float2 acc[8][8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
+
+        for (int kt = seg.k0; kt < seg.k1; ++kt, ++i) {
+            const int s = i % STAGES;
+            if (!mbar_wait(&full[s], (i / STAGES) & 1)) s_abort = 1;
+            const float *sA = smem + s * STAGE_FLOATS;
+            compute_ktile<BN>(sA + (wm0 + tr) * BK, tr, sA + A_FLOATS + wn0 + 4 * tc, acc);
+            __syncthreads();  // every warp is done with stage s
+            if (s_abort) break;
+            if (tid == 0 && prod.template next<BM, BN>(p)) produce();
+        }
+        if (s_abort) break;
+
+        if (seg.k1 < p.KT) {
+            // Not the owner: publish the partial sums of this piece.
+            float4 *slot = p.ws + (static_cast<size_t>(cta) * WARPS + warp) * 1024;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int r = j >> 2, q = j & 3;
+                slot[j * 32 + lane] = make_float4(acc[r][2 * q].x, acc[r][2 * q].y,
+                                                  acc[r][2 * q + 1].x, acc[r][2 * q + 1].y);
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(&p.flags[cta * WARPS + warp], p.epoch);
+            continue;
+        }
+        if (seg.k0 > 0) {
+            // Owner of a split tile: add the pieces of the lower-numbered CTAs that hold
+            // k-iterations [0, k0) of this tile, highest-numbered (latest k) first.
+            const long long tile_begin = static_cast<long long>(seg.tile) * p.KT;
+            for (int c = cta - 1; c >= 0; --c) {
+                if (sk_start(p, c + 1) <= tile_begin) break;  // c's range ends before the tile
+                int ok = 1;
+                if (lane == 0) ok = wait_flag(&p.flags[c * WARPS + warp], p.epoch);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                const float4 *slot = p.ws + (static_cast<size_t>(c) * WARPS + warp) * 1024;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int r = j >> 2, q = j & 3;
+                    const float4 v = __ldcg(slot + j * 32 + lane);
+                    acc[r][2 * q].x += v.x;
+                    acc[r][2 * q].y += v.y;
+                    acc[r][2 * q + 1].x += v.z;
+                    acc[r][2 * q + 1].y += v.w;
+                }
+                if (sk_start(p, c) <= tile_begin) break;  // c started this tile: last piece
+            }
+            // If a contributor never published (its bounded wait expired), the tile is written
+            // without that piece: the output is undefined and the fault word reports it.
+        }
+        epilogue(p.k, p.k.C + static_cast<long long>(b) * p.k.sC, m0 + wm0 + tr,
+                 n0 + wn0 + 4 * tc, acc);
+    }
+
+    if (s_abort && tid == 0) {
+        // Let copies already in flight land before the CTA's shared memory is released.
+        for (; i < issued; ++i)
+            if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1)) break;
+    }
+}
+
 // ---- host side ---------------------------------------------------------------------------
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -372,6 +633,11 @@ const SimtConfig kConfigs[] = {
     {"dp_tma_128x128_s3", 128, 128, 2, 2, 3, kLoaderTma, kScheduleDataParallel},
     {"dp_cpasync_128x256_s4", 128, 256, 2, 4, 4, kLoaderCpAsync, kScheduleDataParallel},
     {"dp_cpasync_128x128_s3", 128, 128, 2, 2, 3, kLoaderCpAsync, kScheduleDataParallel},
+    {"sk_tma_ws_128x256_s4", 128, 256, 2, 4, 4, kLoaderTma, kScheduleStreamK},
+    {"pdp_tma_ws_128x256_s4", 128, 256, 2, 4, 4, kLoaderTma, kSchedulePersistentDP},
+    {"sk_tma_ws_256x128_s4", 256, 128, 4, 2, 4, kLoaderTma, kScheduleStreamK},
+    {"sk_tma_ws_128x128_s3", 128, 128, 2, 2, 3, kLoaderTma, kScheduleStreamK},
+    {"sk_tma_ws_128x128_s4", 128, 128, 2, 2, 4, kLoaderTma, kScheduleStreamK},
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 
@@ -447,6 +713,201 @@ cudaError_t launch_impl(int id, const SimtProblem &p, cudaStream_t stream, const
     return err;
 }
 
+
+// ---- persistent launch: workspace, grid size and the data-parallel / stream-K split ---------
+
+struct WorkspaceEntry {
+    int dev;
+    cudaStream_t stream;
+    void *ptr;
+    size_t bytes;
+    unsigned int epoch;
+};
+std::mutex g_ws_mutex;
+std::vector<WorkspaceEntry> g_ws;
+
+constexpr size_t kFlagBytes = 64 * 1024;  // room for 2048 CTAs x 8 warps of flags
+
+// Workspace for (device, stream): kFlagBytes of flags, then `partial_bytes` of partial sums.
+// Returns the next epoch for this workspace through `epoch`.
+cudaError_t workspace_for(int dev, cudaStream_t stream, size_t partial_bytes, float4 **ws,
+                          unsigned int **flags, unsigned int *epoch) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    WorkspaceEntry *e = nullptr;
+    for (auto &w : g_ws)
+        if (w.dev == dev && w.stream == stream) e = &w;
+    const size_t need = kFlagBytes + partial_bytes;
+    if (e && e->bytes < need) {
+        cudaError_t err = cudaFree(e->ptr);  // waits for work that may still use it
+        e->ptr = nullptr;
+        if (err != cudaSuccess) return err;
+    }
+    if (!e) {
+        g_ws.push_back({dev, stream, nullptr, 0, 0});
+        e = &g_ws.back();
+    }
+    if (!e->ptr) {
+        cudaError_t err = cudaMalloc(&e->ptr, need);
+        if (err != cudaSuccess) {
+            e->ptr = nullptr;
+            e->bytes = 0;
+            return err;
+        }
+        e->bytes = need;
+        e->epoch = 0;
+        err = cudaMemsetAsync(e->ptr, 0, kFlagBytes, stream);
+        if (err != cudaSuccess) return err;
+    }
+    if (++e->epoch == 0) ++e->epoch;
+    *epoch = e->epoch;
+    *flags = static_cast<unsigned int *>(e->ptr);
+    *ws = reinterpret_cast<float4 *>(static_cast<char *>(e->ptr) + kFlagBytes);
+    return cudaSuccess;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+};
+
+int device_sms(int dev) {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 0;
+    if (dev >= 0 && dev < 64) cache[dev] = sms;
+    return sms;
+}
+
+constexpr int kMinItersPerCta = 4;
+
+template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG = 255>
+cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t stream,
+                              const char **detail) {
+    constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
+    constexpr int THREADS = CONSUMER_WARPS * 32;
+    constexpr size_t SMEM = static_cast<size_t>(STAGES) * (BM * BK + BK * BN) * 4 +
+                            2 * STAGES * sizeof(uint64_t) + 1024;
+    auto kernel = simt_gemm_persistent_kernel<BM, BN, WARPS_M, WARPS_N, STAGES, MAXREG>;
+
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) {
+        *detail = "cudaGetDevice failed";
+        return err;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        *detail = "device ordinal above the library's limit";
+        return cudaErrorInvalidDevice;
+    }
+    static std::once_flag attr_once[kMaxDevices];
+    static cudaError_t attr_err[kMaxDevices];
+    static int occupancy[kMaxDevices];
+    std::call_once(attr_once[dev], [&] {
+        attr_err[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(SMEM));
+        if (attr_err[dev] == cudaSuccess)
+            attr_err[dev] = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy[dev], kernel,
+                                                                          THREADS, SMEM);
+    });
+    if (attr_err[dev] != cudaSuccess) {
+        *detail = "kernel attribute / occupancy query failed";
+        return attr_err[dev];
+    }
+    const int sms = device_sms(dev);
+    if (sms <= 0 || occupancy[dev] <= 0) {
+        *detail = "no SM can hold the persistent kernel";
+        return cudaErrorInvalidConfiguration;
+    }
+
+    PParams pp;
+    KParams &kp = pp.k;
+    kp.M = p.M;
+    kp.N = p.N;
+    kp.K = p.K;
+    kp.alpha = p.alpha;
+    kp.beta = p.beta;
+    kp.A = p.A;
+    kp.B = p.B;
+    kp.C = p.C;
+    kp.lda = p.lda;
+    kp.ldb = p.ldb;
+    kp.ldc = p.ldc;
+    kp.sA = p.strideA;
+    kp.sB = p.strideB;
+    kp.sC = p.strideC;
+    kp.batch = p.batch;
+    kp.tiles_m = (p.M + BM - 1) / BM;
+    kp.tiles_n = (p.N + BN - 1) / BN;
+    kp.group_m = 8;
+    kp.a_vec4 = 1;
+    kp.b_vec4 = 1;
+    kp.c_vec4 = operand_vec4(p.C, p.ldc, p.strideC, p.batch);
+
+    const long long tiles_per_batch = static_cast<long long>(kp.tiles_m) * kp.tiles_n;
+    const long long T = tiles_per_batch * p.batch;
+    if (T >= 0x7fffffffLL) {
+        *detail = "too many output tiles";
+        return cudaErrorInvalidValue;
+    }
+    const int KT = (p.K + BK - 1) / BK;
+    const long long g_full = static_cast<long long>(sms) * occupancy[dev];
+    long long dp_tiles = T, G = T < g_full ? T : g_full;
+    if (schedule == kScheduleStreamK && T % g_full != 0) {
+        dp_tiles = T > g_full ? (T / g_full - 1) * g_full : 0;
+        const long long sk_iters = (T - dp_tiles) * KT;
+        if (dp_tiles > 0) {
+            G = g_full;
+        } else {
+            G = sk_iters / kMinItersPerCta;
+            if (G > g_full) G = g_full;
+            if (G < T) G = T;  // never fewer CTAs than tiles
+            if (G > sk_iters) G = sk_iters;
+        }
+        pp.sk_base = sk_iters / G;
+        pp.sk_rem = static_cast<int>(sk_iters % G);
+    } else {
+        pp.sk_base = 0;
+        pp.sk_rem = 0;
+    }
+    pp.KT = KT;
+    pp.tiles_per_batch = static_cast<int>(tiles_per_batch);
+    pp.dp_tiles = static_cast<int>(dp_tiles);
+    pp.G = static_cast<int>(G);
+    pp.ws = nullptr;
+    pp.flags = nullptr;
+    pp.epoch = 1;
+    if (dp_tiles < T) {
+        if (G * CONSUMER_WARPS * sizeof(unsigned int) > kFlagBytes) {
+            *detail = "persistent grid above the workspace's flag capacity";
+            return cudaErrorInvalidConfiguration;
+        }
+        const size_t partial_bytes = static_cast<size_t>(G) * CONSUMER_WARPS * 1024 * sizeof(float4);
+        err = workspace_for(dev, stream, partial_bytes, &pp.ws, &pp.flags, &pp.epoch);
+        if (err != cudaSuccess) {
+            *detail = "stream-K workspace allocation failed";
+            return err;
+        }
+    }
+
+    CUtensorMap mapA, mapB;
+    if (!make_map(&mapA, p.A, p.M, p.K, p.lda, p.strideA, p.batch, BM, BK, true) ||
+        !make_map(&mapB, p.B, p.K, p.N, p.ldb, p.strideB, p.batch, BK, BN, false)) {
+        *detail = "cuTensorMapEncodeTiled rejected an operand";
+        return cudaErrorInvalidValue;
+    }
+    if (const char *env = std::getenv("SGEMM_LOG"); env && *env && env[0] != '0')
+        std::fprintf(stderr,
+                     "[sgemm] persistent %dx%d: occupancy %d, grid %lld, tiles %lld, dp_tiles %lld, "
+                     "k-tiles/tile %d, stream-K iters/CTA %lld (+1 for %d)\n",
+                     BM, BN, occupancy[dev], G, T, dp_tiles, KT, pp.sk_base, pp.sk_rem);
+    kernel<<<static_cast<unsigned>(G), THREADS, SMEM, stream>>>(mapA, mapB, pp);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) *detail = "kernel launch failed";
+    return err;
+}
+
 }  // namespace
 
 int simt_num_configs() { return kNumConfigs; }
@@ -466,11 +927,30 @@ cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const
         case 2: return launch_impl<128, 128, 2, 2, 3, kLoaderTma>(id, p, stream, detail);
         case 3: return launch_impl<128, 256, 2, 4, 4, kLoaderCpAsync>(id, p, stream, detail);
         case 4: return launch_impl<128, 128, 2, 2, 3, kLoaderCpAsync>(id, p, stream, detail);
+        case 5: return launch_persistent<128, 256, 2, 4, 4>(kScheduleStreamK, p, stream, detail);
+        case 6: return launch_persistent<128, 256, 2, 4, 4>(kSchedulePersistentDP, p, stream, detail);
+        case 7: return launch_persistent<256, 128, 4, 2, 4>(kScheduleStreamK, p, stream, detail);
+        case 8: return launch_persistent<128, 128, 2, 2, 3, 248>(kScheduleStreamK, p, stream, detail);
+        case 9: return launch_persistent<128, 128, 2, 2, 4, 248>(kScheduleStreamK, p, stream, detail);
         default: *detail = "unknown SIMT configuration"; return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t release_workspaces() { return cudaSuccess; }
+cudaError_t release_workspaces() {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    cudaError_t first = cudaSuccess;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto &w : g_ws) {
+        if (!w.ptr) continue;
+        cudaSetDevice(w.dev);
+        cudaError_t err = cudaFree(w.ptr);
+        if (err != cudaSuccess && first == cudaSuccess) first = err;
+    }
+    cudaSetDevice(cur);
+    g_ws.clear();
+    return first;
+}
 
 unsigned int simt_take_fault_word(cudaStream_t stream) {
     unsigned int word = 0;

@@ -16,7 +16,8 @@ enum LoaderKind : int {
 // Order in which tiles are assigned to CTAs.
 enum ScheduleKind : int {
     kScheduleDataParallel = 0,  // one CTA per output tile (grouped raster order)
-    kScheduleStreamK = 1,       // persistent CTAs, last partial wave split along K
+    kScheduleStreamK = 1,       // persistent CTAs, the last one-to-two waves split along K
+    kSchedulePersistentDP = 2,  // persistent CTAs, whole tiles round-robin
 };
 
 struct SimtConfig {

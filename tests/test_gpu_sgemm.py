@@ -133,8 +133,9 @@ def test_shape_fuzz(sg, i):
 
 # ---- every configuration of the table ---------------------------------------------------------
 
-@pytest.mark.parametrize("cfg", range(5))
-@pytest.mark.parametrize("shape", [(640, 768, 544), (257, 383, 129), (128, 256, 32)])
+@pytest.mark.parametrize("cfg", range(16))
+@pytest.mark.parametrize("shape", [(640, 768, 544), (257, 383, 129), (128, 256, 32),
+                                   (4096, 2560, 320), (1000, 3000, 2000)])
 def test_each_config(sg, cfg, shape):
     if cfg >= sg.sgemm_num_configs():
         pytest.skip("no such configuration")
@@ -143,6 +144,25 @@ def test_each_config(sg, cfg, shape):
         M, N, K = shape
         _check(Case(M, N, K, 1.5, -0.5, "uniform", seed=cfg), sg)
         got, ref = _check(Case(M, N, K, 1.0, 1.0, "small_int", seed=cfg), sg)
+        assert np.array_equal(got, ref)
+    finally:
+        sg.sgemm_force_config(-1)
+
+
+@pytest.mark.parametrize("name", ["sk_tma_ws_128x256_s4", "sk_tma_ws_256x128_s4",
+                                  "sk_tma_ws_128x128_s3"])
+def test_stream_k_deterministic_and_exact(sg, name):
+    ids = {sg.sgemm_config_name(i): i for i in range(sg.sgemm_num_configs())}
+    sg.sgemm_force_config(ids[name])
+    try:
+        # 4096 x 4096: 512 (or 1024) tiles, a data-parallel phase plus a stream-K tail
+        case = Case(4096, 4096, 4096, 1.0, 0.0, "uniform", seed=11, rows=sample_rows(4096))
+        err, first, ref = run(case, sg.sgemm, torch)
+        assert err <= TOL
+        _, second, _ = run(case, sg.sgemm, torch, check=False)
+        assert np.array_equal(first, second), "stream-K result differs between runs"
+        got, ref = _check(Case(2304, 1792, 1000, 1.0, -1.0, "small_int", seed=12,
+                               rows=sample_rows(2304)), sg)
         assert np.array_equal(got, ref)
     finally:
         sg.sgemm_force_config(-1)
@@ -178,11 +198,17 @@ def _batched(sg, M, N, K, batch, sA, sB, sC, alpha, beta, entry, exact=False):
     del g
 
 
-@pytest.mark.parametrize("M,N,K,batch", [(128, 256, 64, 3), (65, 33, 17, 5), (256, 256, 256, 2)])
-def test_strided_batched(sg, M, N, K, batch):
-    _batched(sg, M, N, K, batch, M * K, K * N, M * N, 0.7, -1.3, sg.sgemm_strided_batched)
-    _batched(sg, M, N, K, batch, M * K, K * N, M * N, 1.0, 1.0, sg.sgemm_strided_batched,
-             exact=True)
+@pytest.mark.parametrize("M,N,K,batch", [(128, 256, 64, 3), (65, 33, 17, 5), (256, 256, 256, 2),
+                                         (512, 768, 300, 7)])
+@pytest.mark.parametrize("cfg", [-1, 5, 6, 8])
+def test_strided_batched(sg, M, N, K, batch, cfg):
+    sg.sgemm_force_config(cfg)
+    try:
+        _batched(sg, M, N, K, batch, M * K, K * N, M * N, 0.7, -1.3, sg.sgemm_strided_batched)
+        _batched(sg, M, N, K, batch, M * K, K * N, M * N, 1.0, 1.0, sg.sgemm_strided_batched,
+                 exact=True)
+    finally:
+        sg.sgemm_force_config(-1)
 
 
 def test_strided_batched_broadcast_and_padding(sg):
