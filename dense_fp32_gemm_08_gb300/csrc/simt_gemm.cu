@@ -860,10 +860,10 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
         if (dp_tiles > 0) {
             G = g_full;
         } else {
+            // at least kMinItersPerCta k-tiles per CTA, never more CTAs than fit at once
             G = sk_iters / kMinItersPerCta;
             if (G > g_full) G = g_full;
-            if (G < T) G = T;  // never fewer CTAs than tiles
-            if (G > sk_iters) G = sk_iters;
+            if (G < 1) G = 1;
         }
         pp.sk_base = sk_iters / G;
         pp.sk_rem = static_cast<int>(sk_iters % G);
