@@ -1,0 +1,116 @@
+"""Host-side logic of bench.py without a GPU: argument rules, the clock-sample parser, the
+ncu-traffic lookup, the CPU-oracle timer and the max-over-ranks reduction of the replica
+runs (two gloo ranks on CPU)."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+sys.path.insert(0, str(ROOT))
+
+import bench  # noqa: E402
+
+
+def test_defaults_and_argument_rules():
+    a = bench.parse([])
+    assert a.gpus == 1 and a.impl == "ours" and a.workload == "headline" and a.warmup >= 3
+    with pytest.raises(SystemExit):
+        bench.parse(["--warmup", "2"])
+    w = bench.WORKLOADS["headline"]
+    assert (w["M"], w["N"], w["K"], w["alpha"], w["beta"]) == (4096, 4096, 4096, 1.0, 0.0)
+    assert 2 * w["M"] * w["N"] * w["K"] == 137_438_953_472
+    for name in ("edge0", "edge1", "edge2", "edge3", "llm_qkv", "llm_up", "llm_down",
+                 "llm_head", "sweep16384", "sq256_ab"):
+        assert name in bench.WORKLOADS
+
+
+def test_clock_summary_parses_reasons():
+    s = bench.ClockSampler(0)
+    s.lines = ["2070, 2070, 900.1, 0x0000000000000000",
+               "1980, 2070, 1390.0, 0x0000000000000004",
+               "2070, 2070, 1200.0, 0x0000000000000000",
+               "garbage"]
+    out = s.summary()
+    assert out["sm_mhz"] == 2070 and out["sm_max_mhz"] == 2070
+    assert out["reasons"] == ["sw_power_cap"] and out["samples"] == 3
+    assert bench.ClockSampler(0).summary()["sm_mhz"] is None
+
+
+def test_ncu_traffic_requires_matching_source(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", tmp_path)
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc").mkdir(parents=True)
+    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "k.cu").write_text("// v1")
+    h = bench.source_hash()
+    data = {"kern@headline": {"dram_bytes_per_launch": 123, "source_hash": h}}
+    (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(data))
+    assert bench.ncu_traffic("kern", "headline") == 123
+    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "k.cu").write_text("// v2")
+    assert bench.ncu_traffic("kern", "headline") is None
+    assert bench.ncu_traffic("other", "headline") is None
+
+
+def test_oracle_timer_counts_rows():
+    import synth
+    w = dict(M=64, N=48, K=32, alpha=1.0, beta=0.5, dist="uniform")
+    A, B, C = synth.uniform(64, 32, 0), synth.uniform(32, 48, 1), synth.uniform(64, 48, 2)
+    t = bench.OracleTimer(w, A, B, C)
+    n = t.rows_for(0.001)
+    assert 1 <= n <= 64
+    dt, rows = t.run(10)
+    assert rows == 10 and dt > 0
+
+
+_CHILD = r"""
+import os, sys
+sys.path.insert(0, {root!r})
+import torch.distributed as dist
+import bench
+dist.init_process_group("gloo")
+rank = dist.get_rank()
+got = bench.max_over_ranks(float(10 + 5 * rank), dist)
+bench.barrier(dist)
+print("RESULT", rank, got, flush=True)
+dist.destroy_process_group()
+"""
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_max_over_ranks_gloo_world_size_2():
+    port = _free_port()
+    procs = []
+    for rank in range(2):
+        env = dict(os.environ, RANK=str(rank), WORLD_SIZE="2", LOCAL_RANK=str(rank),
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, "-c", _CHILD.format(root=str(ROOT))],
+                                      env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                      text=True))
+    outs = [p.communicate(timeout=120) for p in procs]
+    for p, (out, err) in zip(procs, outs):
+        assert p.returncode == 0, err
+    results = sorted(line.split()[1:] for out, _ in outs for line in out.splitlines()
+                     if line.startswith("RESULT"))
+    assert results == [["0", "15.0"], ["1", "15.0"]]
+
+
+def test_reference_arm_runs_on_cpu():
+    proc = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference",
+                           "--workload", "sq256", "--steps", "3", "--warmup", "3",
+                           "--cpu-seconds", "0.5"], capture_output=True, text=True, timeout=300)
+    assert proc.returncode == 0, proc.stderr
+    line = json.loads(proc.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
