@@ -16,7 +16,7 @@ from pathlib import Path
 
 __all__ = [
     "SgemmError", "library_path", "lib", "sgemm", "sgemm_strided_batched", "sgemm_3xtf32",
-    "sgemm_3xtf32_strided_batched", "sgemm_status_string", "sgemm_last_error",
+    "sgemm_3xtf32_strided_batched", "sgemm_noalloc", "sgemm_status_string", "sgemm_last_error",
     "sgemm_device_status", "sgemm_release_workspace", "sgemm_num_configs",
     "sgemm_config_name", "sgemm_select_config", "sgemm_force_config", "matmul",
     "SGEMM_OK", "SGEMM_ERR_INVALID_VALUE", "SGEMM_ERR_LAUNCH", "SGEMM_ERR_TIMEOUT",
@@ -58,7 +58,7 @@ def _bind(L):
     i64, f32, p, i32 = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
     gemm = [i64, i64, i64, f32, p, i64, p, i64, f32, p, i64, p]
     batched = [i64, i64, i64, f32, p, i64, i64, p, i64, i64, f32, p, i64, i64, i64, p]
-    for name, args in (("sgemm", gemm), ("sgemm_3xtf32", gemm),
+    for name, args in (("sgemm", gemm), ("sgemm_3xtf32", gemm), ("sgemm_noalloc", gemm),
                        ("sgemm_strided_batched", batched),
                        ("sgemm_3xtf32_strided_batched", batched)):
         fn = getattr(L, name)
@@ -144,6 +144,12 @@ def sgemm_3xtf32_strided_batched(M, N, K, alpha, A, lda, strideA, B, ldb, stride
     _check(lib().sgemm_3xtf32_strided_batched(M, N, K, alpha, _ptr(A), lda, strideA, _ptr(B),
                                               ldb, strideB, beta, _ptr(C), ldc, strideC, batch,
                                               _stream(stream)))
+
+
+def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:
+    """sgemm() that allocates no device memory (its scratch is a static array in the library)."""
+    _check(lib().sgemm_noalloc(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
+                               _stream(stream)))
 
 
 def sgemm_status_string(status: int) -> str:

@@ -222,6 +222,26 @@ sgemm_status_t sgemm_3xtf32_strided_batched(int64_t M, int64_t N, int64_t K, flo
     return dispatch(a, stream, true);
 }
 
+sgemm_status_t sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                             int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                             int64_t ldc, void *stream_ptr) {
+    Args a{M, N, K, alpha, beta, A, lda, 0, B, ldb, 0, C, ldc, 0, 1};
+    t_last_error[0] = '\0';
+    sgemm_status_t st = validate(a);
+    if (st != SGEMM_OK) return st;
+    if (is_noop(a)) return SGEMM_OK;
+    st = check_limits(a);
+    if (st != SGEMM_OK) return st;
+    if (!have_device()) return fail(SGEMM_ERR_UNSUPPORTED, "no CUDA device available");
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (a.alpha == 0.0f || a.K == 0) return run_scale(a, stream);  // allocates nothing either
+    const char *detail = "";
+    cudaError_t err = sg::simt_launch_noalloc(to_problem(a), stream, &detail);
+    if (err == cudaErrorNotSupported) return fail(SGEMM_ERR_UNSUPPORTED, detail);
+    if (err != cudaSuccess) return fail_cuda(detail, err);
+    return SGEMM_OK;
+}
+
 const char *sgemm_status_string(sgemm_status_t status) {
     switch (status) {
         case SGEMM_OK: return "SGEMM_OK";

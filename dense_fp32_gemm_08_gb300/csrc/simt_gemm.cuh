@@ -57,4 +57,9 @@ unsigned int simt_take_fault_word(cudaStream_t stream);
 // Frees every per-device workspace the SIMT kernels allocated (stream-K partial tiles).
 cudaError_t release_workspaces();
 
+// The stream-K 128 x 256 kernel with its partial sums in a static device array: allocates
+// nothing. Returns cudaErrorNotSupported (with `detail`) when the operands are not TMA-aligned
+// or the call needs more partial-sum slots than the array holds.
+cudaError_t simt_launch_noalloc(const SimtProblem &p, cudaStream_t stream, const char **detail);
+
 }  // namespace sg

@@ -104,6 +104,33 @@ sgemm_status_t sgemm_3xtf32_strided_batched(int64_t M, int64_t N, int64_t K, flo
                                             float beta, float *C, int64_t ldc,
                                             int64_t strideC, int64_t batch, void *stream);
 
+/*
+ * The same product as sgemm(), for callers that must not have the library allocate device
+ * memory: an application that hands its whole memory budget to its own pool, so that a
+ * cudaMalloc from a library would fail or fragment that pool; or code that cannot afford
+ * the device-wide synchronisation that cudaMalloc and cudaFree may cause. The pages have no
+ * counterpart for this entry point.
+ *
+ * It always runs the persistent stream-K kernel with 128 x 256 tiles and keeps that kernel's
+ * partial sums and flags in one array compiled into the library (20 MiB of partial-sum slots
+ * for up to 160 CTAs, plus 8 KiB of flags). Every GPU on which the library is loaded holds
+ * this array until the process exits. It calls no cudaMalloc, cudaFree or other allocating
+ * routine. A, B, C and all conventions are those of sgemm().
+ *
+ * Set-up: the first call on each device looks up that device's copy of the array and sets
+ * the kernel's attributes; make that first call before any stream capture.
+ * Sharing: every call uses the same array, which keeps the previous call's contents; each
+ * call clears the flags it needs, on `stream`, before its kernel runs. Calls whose work
+ * overlaps on the GPU (for example on two streams at once) race on the array and may
+ * produce wrong results: order them on one stream or synchronise between them.
+ * Limits: returns SGEMM_ERR_UNSUPPORTED, with a message naming the need, when its stream-K
+ * schedule would use more than 160 CTAs (more scratch than the array holds), or when A or B
+ * is not 16-byte aligned with lda and ldb multiples of 4.
+ */
+sgemm_status_t sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                             const float *A, int64_t lda, const float *B, int64_t ldb,
+                             float beta, float *C, int64_t ldc, void *stream);
+
 /* Static text for a status code (never NULL). */
 const char *sgemm_status_string(sgemm_status_t status);
 
