@@ -174,27 +174,36 @@ class ClockSampler:
 
 # ---- profiles (ncu traffic figures committed under profiles/) --------------------------------------
 
-def source_hash() -> str:
+KERNEL_SOURCES = {
+    "simt": ("simt_gemm.cu", "simt_gemm.cuh", "ptx.cuh"),
+    "3xtf32": ("tf32x3_gemm.cu", "tf32x3_gemm.cuh", "ptx.cuh"),
+}
+
+
+def source_hash(path: str = "simt") -> str:
+    """Hash of the source files that define a path's kernels (ncu figures go stale with them)."""
     h = hashlib.sha256()
-    for p in sorted((ROOT / "dense_fp32_gemm_08_gb300" / "csrc").glob("*")):
-        if p.suffix in (".cu", ".cuh", ".h"):
-            h.update(p.name.encode())
+    csrc = ROOT / "dense_fp32_gemm_08_gb300" / "csrc"
+    for name in KERNEL_SOURCES[path]:
+        p = csrc / name
+        if p.exists():
+            h.update(name.encode())
             h.update(p.read_bytes())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
+def ncu_traffic(kernel: str, workload: str, path: str = "simt"):
     """DRAM bytes per launch from profiles/ncu_traffic.json, or None when absent or taken on
     a different kernel source."""
-    path = ROOT / "profiles" / "ncu_traffic.json"
-    if not path.exists():
+    fname = ROOT / "profiles" / "ncu_traffic.json"
+    if not fname.exists():
         return None
     try:
-        data = json.loads(path.read_text())
+        data = json.loads(fname.read_text())
     except json.JSONDecodeError:
         return None
     entry = data.get(f"{kernel}@{workload}")
-    if not entry or entry.get("source_hash") != source_hash():
+    if not entry or entry.get("source_hash") != source_hash(path):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -318,7 +327,7 @@ def run_ours(args):
     if args.path == "simt":
         roof = {"bound": "alu", "achieved": round(achieved_tflops, 3), "peak": round(peak_boost, 3),
                 "unit": "TFLOP/s", "frac": round(achieved_tflops / peak_boost, 4),
-                "traffic": ncu_traffic(kernel, args.workload),
+                "traffic": ncu_traffic(kernel, args.workload, "simt"),
                 "peak_basis": f"{sms} SMs x {BOOST_MHZ:.0f} MHz x {FMA_PER_CLK_PER_SM} FMA/clk x 2"}
         if clk.get("sm_mhz"):
             roof["frac_at_run_clock"] = round(
@@ -327,7 +336,7 @@ def run_ours(args):
         roof = {"bound": "tensor", "achieved": round(achieved_tflops, 3),
                 "peak": TF32_DENSE_TFLOPS, "unit": "TFLOP/s",
                 "frac": round(achieved_tflops / TF32_DENSE_TFLOPS, 4),
-                "traffic": ncu_traffic(kernel, args.workload),
+                "traffic": ncu_traffic(kernel, args.workload, "3xtf32"),
                 "peak_basis": "nominal dense TF32 tensor rate; 3 MMAs per algorithmic FLOP issued",
                 "frac_of_fp32_simt_peak": round(achieved_tflops / peak_boost, 4)}
 

@@ -160,8 +160,7 @@ sgemm_status_t run_simt(const Args &a, cudaStream_t stream) {
 sgemm_status_t run_tf32x3(const Args &a, cudaStream_t stream) {
     const sg::SimtProblem p = to_problem(a);
     if (!sg::tf32x3_supports(p))
-        return fail(SGEMM_ERR_UNSUPPORTED,
-                    "3xTF32 path needs 16-byte aligned A, B with lda, ldb (and strides) % 4 == 0");
+        return fail(SGEMM_ERR_UNSUPPORTED, "3xTF32 path takes at most 65535 batch entries");
     const char *detail = "";
     cudaError_t err = sg::tf32x3_launch(p, stream, &detail);
     if (err != cudaSuccess) return fail_cuda(detail, err);
@@ -273,7 +272,9 @@ sgemm_status_t sgemm_release_workspace(void) {
     cudaError_t err = cudaDeviceSynchronize();
     if (err != cudaSuccess) return fail_cuda("device synchronize", err);
     err = sg::release_workspaces();
+    cudaError_t err2 = sg::tf32x3_release_workspaces();
     if (err != cudaSuccess) return fail_cuda("workspace free", err);
+    if (err2 != cudaSuccess) return fail_cuda("split workspace free", err2);
     return SGEMM_OK;
 }
 

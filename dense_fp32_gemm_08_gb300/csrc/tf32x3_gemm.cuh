@@ -7,12 +7,15 @@
 
 namespace sg {
 
-// True when the 3xTF32 kernel can run this problem (16-byte aligned A and B, leading
-// dimensions and batch strides multiples of 4 elements).
+// True when the 3xTF32 kernel can run this problem (any alignment: the split pre-pass reads
+// A and B with plain loads; at most 65535 batch entries).
 bool tf32x3_supports(const SimtProblem &p);
 
 cudaError_t tf32x3_launch(const SimtProblem &p, cudaStream_t stream, const char **detail);
 
 unsigned int tf32x3_take_fault_word(cudaStream_t stream);
+
+// Frees the per-(device, stream) workspaces holding the split operands.
+cudaError_t tf32x3_release_workspaces();
 
 }  // namespace sg

@@ -47,12 +47,14 @@ def test_ncu_traffic_requires_matching_source(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", tmp_path)
     (tmp_path / "profiles").mkdir()
     (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc").mkdir(parents=True)
-    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "k.cu").write_text("// v1")
+    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "simt_gemm.cu").write_text("// v1")
     h = bench.source_hash()
     data = {"kern@headline": {"dram_bytes_per_launch": 123, "source_hash": h}}
     (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(data))
     assert bench.ncu_traffic("kern", "headline") == 123
-    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "k.cu").write_text("// v2")
+    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "tf32x3_gemm.cu").write_text("// other")
+    assert bench.ncu_traffic("kern", "headline") == 123  # another path's file: still valid
+    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "simt_gemm.cu").write_text("// v2")
     assert bench.ncu_traffic("kern", "headline") is None
     assert bench.ncu_traffic("other", "headline") is None
 
