@@ -38,7 +38,8 @@ METRIC = "SGEMM GFLOP/s at 4096³ fp32 and % of GB300 FP32 peak (1 GPU, device-t
 UNIT = "GFLOP/s"
 BOOST_MHZ = 2070.0          # GB300 maximum SM clock (the SIMT peak's clock)
 FMA_PER_CLK_PER_SM = 128    # FP32 lanes per SM
-TF32_DENSE_TFLOPS = 1100.0  # nominal dense TF32 tensor rate of a GB300 (context for 3xTF32)
+TF32_NOMINAL_TFLOPS = 1100.0  # nominal dense TF32 tensor rate of a GB300
+BF16_NOMINAL_TFLOPS = 2250.0  # nominal dense BF16 rate (the ratio scales the measured bf16 peak)
 L2_FLUSH_BYTES = 256 << 20
 
 WORKLOADS = {
@@ -333,11 +334,22 @@ def run_ours(args):
             roof["frac_at_run_clock"] = round(
                 achieved_tflops / (sms * clk["sm_mhz"] * 1e6 * FMA_PER_CLK_PER_SM * 2 / 1e12), 4)
     else:
+        peaks = measured_peaks()
+        if peaks.get("bf16_tflops"):
+            tf32_peak = peaks["bf16_tflops"] * TF32_NOMINAL_TFLOPS / BF16_NOMINAL_TFLOPS
+            basis = (f"measured bf16 {peaks['bf16_tflops']} TFLOP/s x nominal TF32:BF16 "
+                     f"{TF32_NOMINAL_TFLOPS:g}:{BF16_NOMINAL_TFLOPS:g}")
+        else:
+            tf32_peak = TF32_NOMINAL_TFLOPS
+            basis = "nominal dense TF32 rate (no measured peak file)"
         roof = {"bound": "tensor", "achieved": round(achieved_tflops, 3),
-                "peak": TF32_DENSE_TFLOPS, "unit": "TFLOP/s",
-                "frac": round(achieved_tflops / TF32_DENSE_TFLOPS, 4),
+                "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved_tflops / tf32_peak, 4),
+                "issued_tflops": round(3 * achieved_tflops, 3),
+                "issued_frac": round(3 * achieved_tflops / tf32_peak, 4),
                 "traffic": ncu_traffic(kernel, args.workload, "3xtf32"),
-                "peak_basis": "nominal dense TF32 tensor rate; 3 MMAs per algorithmic FLOP issued",
+                "peak_basis": basis + "; achieved counts 2MNK, issued counts the 3 TF32 "
+                                      "products per multiply-add",
                 "frac_of_fp32_simt_peak": round(achieved_tflops / peak_boost, 4)}
 
     e2e = None

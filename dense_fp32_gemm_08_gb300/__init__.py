@@ -18,7 +18,8 @@ __all__ = [
     "SgemmError", "library_path", "lib", "sgemm", "sgemm_strided_batched", "sgemm_3xtf32",
     "sgemm_3xtf32_strided_batched", "sgemm_noalloc", "sgemm_status_string", "sgemm_last_error",
     "sgemm_device_status", "sgemm_release_workspace", "sgemm_num_configs",
-    "sgemm_config_name", "sgemm_select_config", "sgemm_force_config", "matmul",
+    "sgemm_config_name", "sgemm_select_config", "sgemm_force_config",
+    "sgemm_selftest_bounded_wait", "matmul",
     "SGEMM_OK", "SGEMM_ERR_INVALID_VALUE", "SGEMM_ERR_LAUNCH", "SGEMM_ERR_TIMEOUT",
     "SGEMM_ERR_UNSUPPORTED",
 ]
@@ -80,6 +81,8 @@ def _bind(L):
     L.sgemm_select_config.restype = i32
     L.sgemm_force_config.argtypes = [i32]
     L.sgemm_force_config.restype = i32
+    L.sgemm_selftest_bounded_wait.argtypes = [i32, p]
+    L.sgemm_selftest_bounded_wait.restype = i32
     return L
 
 
@@ -185,6 +188,11 @@ def sgemm_select_config(M, N, K, alpha, A, lda, B, ldb, C, ldc, batch=1) -> int:
 
 def sgemm_force_config(i: int) -> None:
     _check(lib().sgemm_force_config(i))
+
+
+def sgemm_selftest_bounded_wait(which: int, stream=None) -> None:
+    """Queue a kernel whose bounded wait expires (failure-path test); see include/sgemm.h."""
+    _check(lib().sgemm_selftest_bounded_wait(which, _stream(stream)))
 
 
 def matmul(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, tensor_cores: bool = False,

@@ -13,6 +13,8 @@
 //                                128x128 CTA per tile has the shortest chain
 //   unaligned (no TMA)           4095x3001x1537: cp.async 128x256 30.1 TF/s        dp_cpasync_128x256_s4
 //                                small shapes: cp.async 128x128                    dp_cpasync_128x128_s3
+//   N <= 8 (any alignment)       4096x1x4096: tile kernels 0.55 ms (HBM-bound)     skinny_tall_n8
+//   M <= 8 (any alignment)       1x4096x4096: tile kernels 0.34 ms (HBM-bound)     skinny_wide_m8
 #pragma once
 
 #include "simt_gemm.cuh"
@@ -30,6 +32,8 @@ enum : int {
     kCfgSkTma256x128 = 7,
     kCfgSkTma128x128s3 = 8,
     kCfgSkTma128x128s4 = 9,
+    kCfgSkinnyTall = 10,
+    kCfgSkinnyWide = 11,
 };
 
 // Waves of 128 x 128 tiles at two CTAs per SM on a 152-SM part.
@@ -40,6 +44,9 @@ inline double waves_128x128(const SimtProblem &p) {
 
 // Picks the configuration id for a problem from its shape class and operand alignment.
 inline int table_choose(const SimtProblem &p) {
+    // One output dimension of at most 8: HBM-bound, the bandwidth kernels (any alignment).
+    if (simt_config_supports(kCfgSkinnyTall, p)) return kCfgSkinnyTall;
+    if (simt_config_supports(kCfgSkinnyWide, p)) return kCfgSkinnyWide;
     const bool tma = simt_config_supports(kCfgDpTma128x128, p);
     const double waves = waves_128x128(p);
     const bool tiny = static_cast<long long>(p.M) * p.N * p.batch <= 128LL * 128;

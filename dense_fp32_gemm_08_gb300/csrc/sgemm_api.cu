@@ -241,6 +241,15 @@ sgemm_status_t sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const
     return SGEMM_OK;
 }
 
+sgemm_status_t sgemm_selftest_bounded_wait(int which, void *stream_ptr) {
+    t_last_error[0] = '\0';
+    if (which != 0 && which != 1) return fail(SGEMM_ERR_INVALID_VALUE, "which must be 0 or 1");
+    if (!have_device()) return fail(SGEMM_ERR_UNSUPPORTED, "no CUDA device available");
+    cudaError_t err = sg::simt_selftest_wait(which, static_cast<cudaStream_t>(stream_ptr));
+    if (err != cudaSuccess) return fail_cuda("self-test kernel launch", err);
+    return SGEMM_OK;
+}
+
 const char *sgemm_status_string(sgemm_status_t status) {
     switch (status) {
         case SGEMM_OK: return "SGEMM_OK";

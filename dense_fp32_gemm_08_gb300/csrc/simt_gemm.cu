@@ -26,6 +26,7 @@
 //    C never read when beta == 0.
 #include "ptx.cuh"
 #include "simt_gemm.cuh"
+#include "skinny_gemm.cuh"
 
 #include <cstdio>
 #include <cstdlib>
@@ -638,6 +639,8 @@ const SimtConfig kConfigs[] = {
     {"sk_tma_ws_256x128_s4", 256, 128, 4, 2, 4, kLoaderTma, kScheduleStreamK},
     {"sk_tma_ws_128x128_s3", 128, 128, 2, 2, 3, kLoaderTma, kScheduleStreamK},
     {"sk_tma_ws_128x128_s4", 128, 128, 2, 2, 4, kLoaderTma, kScheduleStreamK},
+    {"skinny_tall_n8", 0, 0, 0, 0, 0, kLoaderCpAsync, kScheduleSkinny},
+    {"skinny_wide_m8", 0, 0, 0, 0, 0, kLoaderCpAsync, kScheduleSkinny},
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 
@@ -916,6 +919,8 @@ const SimtConfig &simt_config(int id) { return kConfigs[id]; }
 
 bool simt_config_supports(int id, const SimtProblem &p) {
     if (id < 0 || id >= kNumConfigs) return false;
+    if (id == 10) return skinny_supports(kSkinnyTall, p);
+    if (id == 11) return skinny_supports(kSkinnyWide, p);
     if (kConfigs[id].loader == kLoaderTma) return tma_ok(p);
     return true;
 }
@@ -932,6 +937,8 @@ cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const
         case 7: return launch_persistent<256, 128, 4, 2, 4>(kScheduleStreamK, p, stream, detail);
         case 8: return launch_persistent<128, 128, 2, 2, 3, 248>(kScheduleStreamK, p, stream, detail);
         case 9: return launch_persistent<128, 128, 2, 2, 4, 248>(kScheduleStreamK, p, stream, detail);
+        case 10: return skinny_launch(kSkinnyTall, p, stream, detail);
+        case 11: return skinny_launch(kSkinnyWide, p, stream, detail);
         default: *detail = "unknown SIMT configuration"; return cudaErrorInvalidValue;
     }
 }
@@ -1127,6 +1134,32 @@ cudaError_t simt_launch_noalloc(const SimtProblem &p, cudaStream_t stream, const
     err = cudaGetLastError();
     if (err != cudaSuccess) *detail = "kernel launch failed";
     return err;
+}
+
+// ---- failure-path self-test: a bounded wait that can never be satisfied -----------------------
+namespace {
+
+static __device__ unsigned int g_selftest_flag;  // never written: stays 0
+
+// which == 0: waits on an mbarrier phase no thread completes; which == 1: waits for a flag value
+// nothing stores. Both waits give up after kWaitLimitNs, raise the fault word and return.
+__global__ void selftest_wait_kernel(int which) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    if (which == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+        mbar_wait(&bar, 0);
+    } else {
+        wait_flag(&g_selftest_flag, 1u);
+    }
+}
+
+}  // namespace
+
+cudaError_t simt_selftest_wait(int which, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(which);
+    return cudaGetLastError();
 }
 
 }  // namespace sg

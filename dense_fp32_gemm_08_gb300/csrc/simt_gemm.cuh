@@ -15,6 +15,7 @@ enum LoaderKind : int {
 
 // Order in which tiles are assigned to CTAs.
 enum ScheduleKind : int {
+    kScheduleSkinny = -1,       // not a tiled kernel: a bandwidth kernel (skinny_gemm.cu)
     kScheduleDataParallel = 0,  // one CTA per output tile (grouped raster order)
     kScheduleStreamK = 1,       // persistent CTAs, the last one-to-two waves split along K
     kSchedulePersistentDP = 2,  // persistent CTAs, whole tiles round-robin
@@ -56,6 +57,10 @@ unsigned int simt_take_fault_word(cudaStream_t stream);
 
 // Frees every per-device workspace the SIMT kernels allocated (stream-K partial tiles).
 cudaError_t release_workspaces();
+
+// Launches a one-thread kernel whose bounded wait can never be satisfied (which = 0: an
+// mbarrier, 1: a flag word), to exercise the timeout path.
+cudaError_t simt_selftest_wait(int which, cudaStream_t stream);
 
 // The stream-K 128 x 256 kernel with its partial sums in a static device array: allocates
 // nothing. Returns cudaErrorNotSupported (with `detail`) when the operands are not TMA-aligned

@@ -147,6 +147,17 @@ const char *sgemm_last_error(void);
  */
 sgemm_status_t sgemm_device_status(void *stream);
 
+/*
+ * Failure-path self-test (diagnostic, not part of the product's arithmetic). Queues on
+ * `stream` a one-thread kernel whose wait can never be satisfied: which = 0 waits on an
+ * mbarrier phase no thread completes, which = 1 waits for a flag value nothing stores. The
+ * wait is bounded like every wait in the library's kernels: after about 2 s the kernel raises
+ * the device error word and returns, so the next sgemm_device_status(stream) returns
+ * SGEMM_ERR_TIMEOUT and the CUDA context stays usable. Returns SGEMM_ERR_INVALID_VALUE for
+ * another `which`.
+ */
+sgemm_status_t sgemm_selftest_bounded_wait(int which, void *stream);
+
 /* Frees the per-device workspaces: stream-K partial sums and 3xTF32 split operands (the
  * next call that needs one allocates it again). Synchronises the device first. */
 sgemm_status_t sgemm_release_workspace(void);

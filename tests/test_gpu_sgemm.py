@@ -131,6 +131,27 @@ def test_shape_fuzz(sg, i):
                 ldc_pad=pads[2], a_off=offs[0], b_off=offs[1], c_off=offs[2]), sg)
 
 
+# ---- skinny shapes: one output dimension of at most 8 (bandwidth kernels) ------------------------
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (2, 1000, 3000), (3, 257, 129), (5, 3001, 77),
+                                   (8, 4097, 1025), (4096, 1, 4096), (1000, 2, 3000),
+                                   (257, 3, 129), (3001, 7, 77), (4097, 8, 1025), (1, 1, 5000),
+                                   (7, 5, 33)])
+@pytest.mark.parametrize("pad,off", [(0, 0), (3, 1)])
+def test_skinny_shapes(sg, M, N, K, pad, off):
+    _check(Case(M, N, K, 0.7, -1.3, "normal", seed=M + N, lda_pad=pad, ldb_pad=pad, ldc_pad=pad,
+                a_off=off, b_off=off, c_off=off), sg)
+    got, ref = _check(Case(M, N, K, 1.0, 1.0, "small_int", seed=M * N, lda_pad=pad,
+                           a_off=off, b_off=off), sg)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("M,N,K,batch", [(1, 640, 300, 4), (500, 3, 200, 3)])
+def test_skinny_strided_batched(sg, M, N, K, batch):
+    _batched(sg, M, N, K, batch, M * K + 8, K * N + 4, M * N + 4, 0.7, -1.3,
+             sg.sgemm_strided_batched)
+
+
 # ---- every configuration of the table ---------------------------------------------------------
 
 @pytest.mark.parametrize("cfg", range(16))
