@@ -113,6 +113,15 @@ def test_config_table_names(sgemm_lib):
     assert sgemm_lib.sgemm_config_name(-1) is None
 
 
+def test_skinny_shapes_select_bandwidth_kernels(sgemm_lib):
+    sel = sgemm_lib.sgemm_select_config
+    name = sgemm_lib.sgemm_config_name
+    assert name(sel(4096, 1, 4096, 1.0, FAKE, 4096, FAKE, 1, FAKE, 1)).startswith("skinny_tall")
+    assert name(sel(1, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096)).startswith("skinny_wide")
+    assert name(sel(8, 9, 64, 1.0, FAKE + 4, 64, FAKE, 9, FAKE, 9)).startswith("skinny_wide")
+    assert not name(sel(9, 9, 64, 1.0, FAKE, 64, FAKE, 12, FAKE, 12)).startswith("skinny")
+
+
 def test_selection_follows_alignment(sgemm_lib):
     sel = sgemm_lib.sgemm_select_config
     name = sgemm_lib.sgemm_config_name
@@ -132,8 +141,21 @@ def test_force_config(sgemm_lib):
         n = sgemm_lib.sgemm_num_configs()
         for i in range(n):
             sgemm_lib.sgemm_force_config(i)
-            got = sel(512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512)
-            assert got == i
+            name = sgemm_lib.sgemm_config_name(i)
+            if name.startswith("skinny_tall"):
+                shape = (512, 3, 512)
+            elif name.startswith("skinny_wide"):
+                shape = (3, 512, 512)
+            else:
+                shape = (512, 512, 512)
+            M, N, K = shape
+            got = sel(M, N, K, 1.0, FAKE, K, FAKE, N, FAKE, N)
+            assert got == i, name
+        # a forced skinny kernel cannot take a square problem: the table decides instead
+        sgemm_lib.sgemm_force_config([i for i in range(n)
+                                      if sgemm_lib.sgemm_config_name(i).startswith("skinny")][0])
+        assert not sgemm_lib.sgemm_config_name(
+            sel(512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512)).startswith("skinny")
         # a TMA configuration cannot take a misaligned operand: the table decides instead
         tma_ids = [i for i in range(n) if "tma" in sgemm_lib.sgemm_config_name(i)]
         sgemm_lib.sgemm_force_config(tma_ids[0])
