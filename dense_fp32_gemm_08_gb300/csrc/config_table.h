@@ -11,8 +11,10 @@
 //                                16384x12288x4096: dp 128x128 65.3, sk 62.7
 //   aligned, one tile or less    256^3 and below: latency bound, a single          dp_tma_128x128_s3
 //                                128x128 CTA per tile has the shortest chain
-//   unaligned (no TMA)           4095x3001x1537: cp.async 128x256 30.1 TF/s        dp_cpasync_128x256_s4
-//                                small shapes: cp.async 128x128                    dp_cpasync_128x128_s3
+//   unaligned (no TMA)           4095x3001x1537: dp cp.async 128x256 30.1 TF/s,    packed_sk_tma_128x256_s4
+//                                sk cp.async 128x256 35.2; 127x129x4099: dp        (packed_dp_tma_128x128_s3
+//                                cp.async 0.72 ms, sk cp.async 0.10 ms             at >= 6 waves)
+//   unaligned, broadcast batch   operands that cannot be repacked once             sk_cpasync_128x256_s4
 //   N <= 8 (any alignment)       4096x1x4096: tile kernels 0.55 ms (HBM-bound)     skinny_tall_n8
 //   M <= 8 (any alignment)       1x4096x4096: tile kernels 0.34 ms (HBM-bound)     skinny_wide_m8
 #pragma once
@@ -34,6 +36,10 @@ enum : int {
     kCfgSkTma128x128s4 = 9,
     kCfgSkinnyTall = 10,
     kCfgSkinnyWide = 11,
+    kCfgSkCp128x256 = 12,
+    kCfgSkCp256x128 = 13,
+    kCfgPackedSk128x256 = 14,
+    kCfgPackedDp128x128 = 15,
 };
 
 // Waves of 128 x 128 tiles at two CTAs per SM on a 152-SM part.
@@ -50,7 +56,11 @@ inline int table_choose(const SimtProblem &p) {
     const bool tma = simt_config_supports(kCfgDpTma128x128, p);
     const double waves = waves_128x128(p);
     const bool tiny = static_cast<long long>(p.M) * p.N * p.batch <= 128LL * 128;
-    if (!tma) return static_cast<long long>(p.M) * p.N <= 512LL * 512 ? kCfgDpCp128x128 : kCfgDpCp128x256;
+    if (!tma) {
+        if (simt_config_supports(kCfgPackedSk128x256, p))
+            return waves >= 6.0 ? kCfgPackedDp128x128 : kCfgPackedSk128x256;
+        return waves >= 6.0 ? kCfgDpCp128x128 : kCfgSkCp128x256;
+    }
     if (tiny) return kCfgDpTma128x128;
     if (waves >= 6.0) return kCfgDpTma128x128;
     return kCfgSkTma128x256;

@@ -55,17 +55,17 @@ bool log_enabled() {
     return on;
 }
 
-// C = beta * C (zeros when beta == 0, C not read then). Grid-stride over batch x M x N.
+// C = beta * C (zeros when beta == 0, C not read then). Rows over the grid's y dimension
+// (batch entries stacked), columns over threads.
 __global__ void scale_c_kernel(float *C, long long M, long long N, long long ldc,
                                long long strideC, long long batch, float beta) {
-    const long long per = M * N;
-    const long long total = per * batch;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long b = i / per, rem = i - b * per;
-        const long long r = rem / N, c = rem - r * N;
-        float *p = C + b * strideC + r * ldc + c;
-        *p = beta == 0.0f ? 0.0f : beta * *p;
+    const long long nrows = M * batch;
+    for (long long gr = blockIdx.y; gr < nrows; gr += gridDim.y) {
+        const long long b = gr / M, r = gr - b * M;
+        float *row = C + b * strideC + r * ldc;
+        for (long long c = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; c < N;
+             c += static_cast<long long>(gridDim.x) * blockDim.x)
+            row[c] = beta == 0.0f ? 0.0f : beta * row[c];
     }
 }
 
@@ -108,12 +108,10 @@ sgemm_status_t check_limits(const Args &a) {
 }
 
 sgemm_status_t run_scale(const Args &a, cudaStream_t stream) {
-    const long long total = a.M * a.N * a.batch;
-    const int threads = 256;
-    long long blocks = (total + threads - 1) / threads;
-    if (blocks > 152LL * 32) blocks = 152LL * 32;
-    scale_c_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a.C, a.M, a.N, a.ldc,
-                                                                          a.sC, a.batch, a.beta);
+    const long long nrows = a.M * a.batch;
+    const dim3 grid(static_cast<unsigned>((a.N + 255) / 256 < 8 ? (a.N + 255) / 256 : 8),
+                    static_cast<unsigned>(nrows < 65535 ? nrows : 65535));
+    scale_c_kernel<<<grid, 256, 0, stream>>>(a.C, a.M, a.N, a.ldc, a.sC, a.batch, a.beta);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return fail_cuda("scale kernel launch", err);
     return SGEMM_OK;
@@ -281,7 +279,9 @@ sgemm_status_t sgemm_release_workspace(void) {
     cudaError_t err = cudaDeviceSynchronize();
     if (err != cudaSuccess) return fail_cuda("device synchronize", err);
     err = sg::release_workspaces();
+    cudaError_t err3 = sg::release_pack_workspaces();
     cudaError_t err2 = sg::tf32x3_release_workspaces();
+    if (err == cudaSuccess) err = err3;
     if (err != cudaSuccess) return fail_cuda("workspace free", err);
     if (err2 != cudaSuccess) return fail_cuda("split workspace free", err2);
     return SGEMM_OK;

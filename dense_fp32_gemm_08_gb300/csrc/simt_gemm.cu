@@ -30,6 +30,7 @@
 
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -448,7 +449,8 @@ struct TmaProducer {
 
 // MAXREG caps registers per thread: four-warp tiles run two CTAs per SM and must leave room
 // for both in the register file.
-template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG>
+template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG,
+          int LOADER = kLoaderTma>
 __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
     simt_gemm_persistent_kernel(const __grid_constant__ CUtensorMap mapA,
                                 const __grid_constant__ CUtensorMap mapB, const PParams p) {
@@ -470,29 +472,48 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
 
     if (tid == 0) {
         s_abort = 0;
-        tma_prefetch_desc(&mapA);
-        tma_prefetch_desc(&mapB);
+        if (LOADER == kLoaderTma) {
+            tma_prefetch_desc(&mapA);
+            tma_prefetch_desc(&mapB);
 #pragma unroll
-        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
-        mbar_init_fence();
+            for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+            mbar_init_fence();
+        }
     }
     __syncthreads();
 
-    // Thread 0 streams the k-tiles of the CTA's whole segment list into the ring: the first
-    // STAGES up front, then one refill into the stage just released after every k-tile.
+    // TMA: thread 0 streams the k-tiles of the CTA's whole segment list into the ring, the
+    // first STAGES up front, then one refill into the stage just released after every k-tile.
+    // cp.async: every thread walks the same cursor and copies its share of each k-tile; the
+    // first STAGES - 1 up front, then, after the barrier that ends k-tile i - 1, k-tile
+    // i + STAGES - 1 into the stage k-tile i - 1 used.
     TmaProducer prod(p, cta);
     int issued = 0;
     auto produce = [&]() {
         const int s = issued % STAGES;
         float *sA = smem + s * STAGE_FLOATS;
-        mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-        tma_load_3d(sA, &mapA, &full[s], prod.kt * BK, prod.m0, prod.b);
-        tma_load_3d(sA + A_FLOATS, &mapB, &full[s], prod.n0, prod.kt * BK, prod.b);
+        if (LOADER == kLoaderTma) {
+            mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+            tma_load_3d(sA, &mapA, &full[s], prod.kt * BK, prod.m0, prod.b);
+            tma_load_3d(sA + A_FLOATS, &mapB, &full[s], prod.n0, prod.kt * BK, prod.b);
+        } else {
+            cp_async_stage<BM, BN, WARPS * 32>(
+                sA, sA + A_FLOATS, p.k, p.k.A + static_cast<long long>(prod.b) * p.k.sA,
+                p.k.B + static_cast<long long>(prod.b) * p.k.sB, prod.m0, prod.n0, prod.kt * BK,
+                tid);
+        }
         ++prod.kt;
         ++issued;
     };
-    if (tid == 0)
-        while (issued < STAGES && prod.template next<BM, BN>(p)) produce();
+    if (LOADER == kLoaderTma) {
+        if (tid == 0)
+            while (issued < STAGES && prod.template next<BM, BN>(p)) produce();
+    } else {
+        for (int s = 0; s < STAGES - 1; ++s) {
+            if (prod.template next<BM, BN>(p)) produce();
+            cp_async_commit();
+        }
+    }
 
     const int wm0 = (warp / WARPS_N) * 64, wn0 = (warp % WARPS_N) * 64;
     const int tr = lane >> 2, tc = lane & 3;
@@ -510,12 +531,21 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
 
         for (int kt = seg.k0; kt < seg.k1; ++kt, ++i) {
             const int s = i % STAGES;
-            if (!mbar_wait(&full[s], (i / STAGES) & 1)) s_abort = 1;
+            if (LOADER == kLoaderTma) {
+                if (!mbar_wait(&full[s], (i / STAGES) & 1)) s_abort = 1;
+            } else {
+                cp_async_wait<STAGES - 2>();
+                __syncthreads();  // k-tile i landed for all threads; k-tile i - 1's stage is free
+                if (prod.template next<BM, BN>(p)) produce();
+                cp_async_commit();
+            }
             const float *sA = smem + s * STAGE_FLOATS;
             compute_ktile<BN>(sA + (wm0 + tr) * BK, tr, sA + A_FLOATS + wn0 + 4 * tc, acc);
-            __syncthreads();  // every warp is done with stage s
-            if (s_abort) break;
-            if (tid == 0 && prod.template next<BM, BN>(p)) produce();
+            if (LOADER == kLoaderTma) {
+                __syncthreads();  // every warp is done with stage s
+                if (s_abort) break;
+                if (tid == 0 && prod.template next<BM, BN>(p)) produce();
+            }
         }
         if (s_abort) break;
 
@@ -562,7 +592,8 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
                  n0 + wn0 + 4 * tc, acc);
     }
 
-    if (s_abort && tid == 0) {
+    if (LOADER != kLoaderTma) cp_async_wait<0>();
+    if (LOADER == kLoaderTma && s_abort && tid == 0) {
         // Let copies already in flight land before the CTA's shared memory is released.
         for (; i < issued; ++i)
             if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1)) break;
@@ -641,6 +672,10 @@ const SimtConfig kConfigs[] = {
     {"sk_tma_ws_128x128_s4", 128, 128, 2, 2, 4, kLoaderTma, kScheduleStreamK},
     {"skinny_tall_n8", 0, 0, 0, 0, 0, kLoaderCpAsync, kScheduleSkinny},
     {"skinny_wide_m8", 0, 0, 0, 0, 0, kLoaderCpAsync, kScheduleSkinny},
+    {"sk_cpasync_128x256_s4", 128, 256, 2, 4, 4, kLoaderCpAsync, kScheduleStreamK},
+    {"sk_cpasync_256x128_s4", 256, 128, 4, 2, 4, kLoaderCpAsync, kScheduleStreamK},
+    {"packed_sk_tma_128x256_s4", 128, 256, 2, 4, 4, kLoaderTma, kScheduleStreamK},
+    {"packed_dp_tma_128x128_s3", 128, 128, 2, 2, 3, kLoaderTma, kScheduleDataParallel},
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 
@@ -785,14 +820,15 @@ int device_sms(int dev) {
 
 constexpr int kMinItersPerCta = 4;
 
-template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG = 255>
+template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG = 255,
+          int LOADER = kLoaderTma>
 cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t stream,
                               const char **detail) {
     constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
     constexpr int THREADS = CONSUMER_WARPS * 32;
     constexpr size_t SMEM = static_cast<size_t>(STAGES) * (BM * BK + BK * BN) * 4 +
                             2 * STAGES * sizeof(uint64_t) + 1024;
-    auto kernel = simt_gemm_persistent_kernel<BM, BN, WARPS_M, WARPS_N, STAGES, MAXREG>;
+    auto kernel = simt_gemm_persistent_kernel<BM, BN, WARPS_M, WARPS_N, STAGES, MAXREG, LOADER>;
 
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -844,8 +880,8 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
     kp.tiles_m = (p.M + BM - 1) / BM;
     kp.tiles_n = (p.N + BN - 1) / BN;
     kp.group_m = 8;
-    kp.a_vec4 = 1;
-    kp.b_vec4 = 1;
+    kp.a_vec4 = operand_vec4(p.A, p.lda, p.strideA, p.batch);
+    kp.b_vec4 = operand_vec4(p.B, p.ldb, p.strideB, p.batch);
     kp.c_vec4 = operand_vec4(p.C, p.ldc, p.strideC, p.batch);
 
     const long long tiles_per_batch = static_cast<long long>(kp.tiles_m) * kp.tiles_n;
@@ -895,8 +931,11 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
     }
 
     CUtensorMap mapA, mapB;
-    if (!make_map(&mapA, p.A, p.M, p.K, p.lda, p.strideA, p.batch, BM, BK, true) ||
-        !make_map(&mapB, p.B, p.K, p.N, p.ldb, p.strideB, p.batch, BK, BN, false)) {
+    memset(&mapA, 0, sizeof(mapA));
+    memset(&mapB, 0, sizeof(mapB));
+    if (LOADER == kLoaderTma &&
+        (!make_map(&mapA, p.A, p.M, p.K, p.lda, p.strideA, p.batch, BM, BK, true) ||
+         !make_map(&mapB, p.B, p.K, p.N, p.ldb, p.strideB, p.batch, BK, BN, false))) {
         *detail = "cuTensorMapEncodeTiled rejected an operand";
         return cudaErrorInvalidValue;
     }
@@ -911,6 +950,10 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
     return err;
 }
 
+bool packable(const SimtProblem &p);
+cudaError_t launch_packed(int inner, const SimtProblem &p, cudaStream_t stream,
+                          const char **detail);
+
 }  // namespace
 
 int simt_num_configs() { return kNumConfigs; }
@@ -921,6 +964,7 @@ bool simt_config_supports(int id, const SimtProblem &p) {
     if (id < 0 || id >= kNumConfigs) return false;
     if (id == 10) return skinny_supports(kSkinnyTall, p);
     if (id == 11) return skinny_supports(kSkinnyWide, p);
+    if (id == 14 || id == 15) return packable(p);
     if (kConfigs[id].loader == kLoaderTma) return tma_ok(p);
     return true;
 }
@@ -939,6 +983,14 @@ cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const
         case 9: return launch_persistent<128, 128, 2, 2, 4, 248>(kScheduleStreamK, p, stream, detail);
         case 10: return skinny_launch(kSkinnyTall, p, stream, detail);
         case 11: return skinny_launch(kSkinnyWide, p, stream, detail);
+        case 12:
+            return launch_persistent<128, 256, 2, 4, 4, 255, kLoaderCpAsync>(kScheduleStreamK, p,
+                                                                            stream, detail);
+        case 13:
+            return launch_persistent<256, 128, 4, 2, 4, 255, kLoaderCpAsync>(kScheduleStreamK, p,
+                                                                            stream, detail);
+        case 14: return launch_packed(5, p, stream, detail);
+        case 15: return launch_packed(2, p, stream, detail);
         default: *detail = "unknown SIMT configuration"; return cudaErrorInvalidValue;
     }
 }
@@ -1160,6 +1212,145 @@ __global__ void selftest_wait_kernel(int which) {
 cudaError_t simt_selftest_wait(int which, cudaStream_t stream) {
     selftest_wait_kernel<<<1, 32, 0, stream>>>(which);
     return cudaGetLastError();
+}
+
+// ---- repacking operands TMA cannot read -------------------------------------------------------
+//
+// TMA needs 16-byte aligned rows (base and leading dimension). An operand without them is
+// copied once into a workspace with its leading dimension rounded up to a multiple of 4,
+// then the TMA kernels run on the copy: the copy streams the operand at HBM speed, which
+// is cheaper than feeding every k-tile through 4-byte cp.async copies.
+namespace {
+
+// Rows run over the grid's y dimension (batch entries stacked), columns over threads.
+__global__ void pack_rows_kernel(const float *__restrict__ src, long long lds, long long ss,
+                                 float *__restrict__ dst, long long ldd, long long sd, int rows,
+                                 int cols, int batch) {
+    const long long nrows = static_cast<long long>(rows) * batch;
+    for (long long gr = blockIdx.y; gr < nrows; gr += gridDim.y) {
+        const long long b = gr / rows, r = gr - b * rows;
+        const float *s = src + b * ss + r * lds;
+        float *d = dst + b * sd + r * ldd;
+        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x)
+            d[c] = s[c];
+    }
+}
+
+dim3 rows_grid(long long rows, int cols) {
+    const unsigned x = static_cast<unsigned>(std::min<long long>((cols + 255) / 256, 8));
+    const unsigned y = static_cast<unsigned>(std::min<long long>(rows, 65535));
+    return dim3(x, y);
+}
+
+struct PackWorkspace {
+    int dev;
+    cudaStream_t stream;
+    void *ptr;
+    size_t bytes;
+};
+std::mutex g_pack_mutex;
+std::vector<PackWorkspace> g_pack_ws;
+
+cudaError_t pack_workspace(int dev, cudaStream_t stream, size_t bytes, float **out) {
+    std::lock_guard<std::mutex> lock(g_pack_mutex);
+    PackWorkspace *e = nullptr;
+    for (auto &w : g_pack_ws)
+        if (w.dev == dev && w.stream == stream) e = &w;
+    if (e && e->bytes < bytes) {
+        cudaError_t err = cudaFree(e->ptr);
+        e->ptr = nullptr;
+        e->bytes = 0;
+        if (err != cudaSuccess) return err;
+    }
+    if (!e) {
+        g_pack_ws.push_back({dev, stream, nullptr, 0});
+        e = &g_pack_ws.back();
+    }
+    if (!e->ptr) {
+        cudaError_t err = cudaMalloc(&e->ptr, bytes);
+        if (err != cudaSuccess) {
+            e->ptr = nullptr;
+            return err;
+        }
+        e->bytes = bytes;
+    }
+    *out = static_cast<float *>(e->ptr);
+    return cudaSuccess;
+}
+
+bool packable(const SimtProblem &p) {
+    // a broadcast operand (batch stride 0) would need one copy per batch entry: not packed
+    return p.batch <= 1 || (p.strideA != 0 && p.strideB != 0);
+}
+
+cudaError_t launch_packed(int inner, const SimtProblem &p, cudaStream_t stream,
+                          const char **detail) {
+    const bool packA = !operand_vec4(p.A, p.lda, p.strideA, p.batch);
+    const bool packB = !operand_vec4(p.B, p.ldb, p.strideB, p.batch);
+    const long long ldA = (static_cast<long long>(p.K) + 3) / 4 * 4;
+    const long long ldB = (static_cast<long long>(p.N) + 3) / 4 * 4;
+    const long long elemsA = packA ? static_cast<long long>(p.M) * ldA : 0;
+    const long long elemsB = packB ? static_cast<long long>(p.K) * ldB : 0;
+    SimtProblem q = p;
+    if (packA || packB) {
+        int dev = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) {
+            *detail = "cudaGetDevice failed";
+            return err;
+        }
+        float *ws = nullptr;
+        err = pack_workspace(dev, stream, static_cast<size_t>(elemsA + elemsB) * p.batch * 4, &ws);
+        if (err != cudaSuccess) {
+            *detail = "repacking workspace allocation failed";
+            return err;
+        }
+        if (packA) {
+            pack_rows_kernel<<<rows_grid(static_cast<long long>(p.M) * p.batch, p.K), 256, 0,
+                               stream>>>(p.A, p.lda, p.strideA, ws, ldA, elemsA, p.M, p.K,
+                                         p.batch);
+            q.A = ws;
+            q.lda = ldA;
+            q.strideA = p.batch > 1 ? elemsA : 0;
+        }
+        if (packB) {
+            float *wb = ws + elemsA * p.batch;
+            pack_rows_kernel<<<rows_grid(static_cast<long long>(p.K) * p.batch, p.N), 256, 0,
+                               stream>>>(p.B, p.ldb, p.strideB, wb, ldB, elemsB, p.K, p.N,
+                                         p.batch);
+            q.B = wb;
+            q.ldb = ldB;
+            q.strideB = p.batch > 1 ? elemsB : 0;
+        }
+        err = cudaGetLastError();
+        if (err != cudaSuccess) {
+            *detail = "repacking kernel launch failed";
+            return err;
+        }
+    }
+    if (!tma_ok(q)) {
+        *detail = "operands not readable by TMA after repacking";
+        return cudaErrorInvalidValue;
+    }
+    return simt_launch(inner, q, stream, detail);
+}
+
+}  // namespace
+
+cudaError_t release_pack_workspaces() {
+    std::lock_guard<std::mutex> lock(g_pack_mutex);
+    cudaError_t first = cudaSuccess;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto &w : g_pack_ws) {
+        if (!w.ptr) continue;
+        cudaSetDevice(w.dev);
+        cudaError_t err = cudaFree(w.ptr);
+        if (err != cudaSuccess && first == cudaSuccess) first = err;
+    }
+    cudaSetDevice(cur);
+    g_pack_ws.clear();
+    return first;
 }
 
 }  // namespace sg

@@ -58,6 +58,9 @@ unsigned int simt_take_fault_word(cudaStream_t stream);
 // Frees every per-device workspace the SIMT kernels allocated (stream-K partial tiles).
 cudaError_t release_workspaces();
 
+// Frees the per-(device, stream) copies of operands repacked for TMA.
+cudaError_t release_pack_workspaces();
+
 // Launches a one-thread kernel whose bounded wait can never be satisfied (which = 0: an
 // mbarrier, 1: a flag word), to exercise the timeout path.
 cudaError_t simt_selftest_wait(int which, cudaStream_t stream);

@@ -7,8 +7,8 @@
 //   float4 (or scalar) chunks of the row, multiplies them by the matching rows of B (K x N,
 //   small and L1/L2-resident), and keeps N partial sums; a shuffle tree in fixed lane order
 //   reduces them. Every row is independent; M rows give M warps of work.
-// * M <= 8 ("wide"): the large operand is B (K x N). A CTA of 4 warps owns 128 columns of C;
-//   its 8-CTA cluster splits K into 8 ranges, and within a CTA warp w takes k = w, w + 4, ...
+// * M <= 8 ("wide"): the large operand is B (K x N). A CTA of 8 warps owns 128 columns of C;
+//   its 8-CTA cluster splits K into 8 ranges, and within a CTA warp w takes k = w, w + 8, ...
 //   of its range, so every warp streams whole 512-byte row segments of B. Partial sums are
 //   reduced over the warps through shared memory and over the cluster through distributed
 //   shared memory, both in a fixed order; the cluster's CTA 0 applies alpha / beta. No
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(256) skinny_tall_kernel(SkinnyProblem p) {
 // ---- wide: M <= 8 --------------------------------------------------------------------------------
 
 constexpr int kWideCols = 128;   // columns of C per CTA (32 lanes x float4)
-constexpr int kWideWarps = 4;
+constexpr int kWideWarps = 8;
 constexpr int kCluster = 8;      // CTAs per cluster, splitting K
 
 template <int MM, bool VEC>
@@ -96,7 +96,7 @@ __global__ void __cluster_dims__(1, kCluster, 1) __launch_bounds__(kWideWarps * 
     const int rank = static_cast<int>(cluster.block_rank());  // position along K
     const int b = blockIdx.z;
     const int n0 = blockIdx.x * kWideCols + 4 * lane;
-    // K range of this CTA: a multiple of 4 so that warps interleave whole k values.
+    // K range of this CTA (rounded up to a multiple of 4).
     const int kper = ((p.K + kCluster - 1) / kCluster + 3) & ~3;
     const int kb = rank * kper;
     const int ke = min(p.K, kb + kper);
@@ -107,7 +107,7 @@ __global__ void __cluster_dims__(1, kCluster, 1) __launch_bounds__(kWideWarps * 
 #pragma unroll
     for (int m = 0; m < MM; ++m) acc[m] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     const bool full = n0 + 3 < p.N;
-#pragma unroll 4
+#pragma unroll 8
     for (int k = kb + warp; k < ke; k += kWideWarps) {
         const float *brow = B + static_cast<long long>(k) * p.ldb + n0;
         float4 bv;

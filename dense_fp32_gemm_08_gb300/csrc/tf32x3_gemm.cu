@@ -29,6 +29,7 @@
 #include "ptx.cuh"
 #include "tf32x3_gemm.cuh"
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -53,20 +54,22 @@ __device__ __forceinline__ void split_value(float x, float &big, float &small) {
 }
 
 // A (rows x cols, leading dimension lda, batch stride sA) -> big, small (rows x ldo each,
-// batch stride so), same orientation.
+// batch stride so), same orientation. Rows over the grid's y dimension, columns over threads.
 __global__ void split_rows_kernel(const float *__restrict__ A, long long lda, long long sA,
                                   float *__restrict__ big, float *__restrict__ small,
                                   long long ldo, long long so, int rows, int cols, int batch) {
-    const long long per = static_cast<long long>(rows) * cols;
-    const long long total = per * batch;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long b = i / per, rem = i - b * per;
-        const long long r = rem / cols, c = rem - r * cols;
-        float hi, lo;
-        split_value(A[b * sA + r * lda + c], hi, lo);
-        big[b * so + r * ldo + c] = hi;
-        small[b * so + r * ldo + c] = lo;
+    const long long nrows = static_cast<long long>(rows) * batch;
+    for (long long gr = blockIdx.y; gr < nrows; gr += gridDim.y) {
+        const long long b = gr / rows, r = gr - b * rows;
+        const float *src = A + b * sA + r * lda;
+        float *hi = big + b * so + r * ldo;
+        float *lo = small + b * so + r * ldo;
+        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x) {
+            float h, l;
+            split_value(src[c], h, l);
+            hi[c] = h;
+            lo[c] = l;
+        }
     }
 }
 
@@ -447,11 +450,11 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
     float *b_lo = b_hi + b_elems * p.batch;
 
     {
-        const long long total = static_cast<long long>(p.M) * p.K * p.batch;
-        long long blocks = (total + 255) / 256;
-        if (blocks > 152LL * 16) blocks = 152LL * 16;
-        split_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.M, p.K, p.batch);
+        const long long nrows = static_cast<long long>(p.M) * p.batch;
+        const dim3 rgrid(static_cast<unsigned>(std::min<long long>((p.K + 255) / 256, 8)),
+                         static_cast<unsigned>(std::min<long long>(nrows, 65535)));
+        split_rows_kernel<<<rgrid, 256, 0, stream>>>(p.A, p.lda, p.strideA, a_hi, a_lo, ldk,
+                                                     a_elems, p.M, p.K, p.batch);
         err = cudaGetLastError();
         if (err != cudaSuccess) {
             *detail = "split kernel launch failed";

@@ -127,8 +127,9 @@ def test_selection_follows_alignment(sgemm_lib):
     name = sgemm_lib.sgemm_config_name
     aligned = name(sel(4096, 4096, 4096, 1.0, FAKE, 4096, FAKE, 4096, FAKE, 4096))
     assert "tma" in aligned
-    assert "cpasync" in name(sel(4096, 4096, 4096, 1.0, FAKE + 4, 4096, FAKE, 4096, FAKE, 4096))
-    assert "cpasync" in name(sel(4095, 3001, 1537, 1.0, FAKE, 1537, FAKE, 3001, FAKE, 3001))
+    # operands TMA cannot read are repacked (or, failing that, loaded with cp.async)
+    assert "packed" in name(sel(4096, 4096, 4096, 1.0, FAKE + 4, 4096, FAKE, 4096, FAKE, 4096))
+    assert "packed" in name(sel(4095, 3001, 1537, 1.0, FAKE, 1537, FAKE, 3001, FAKE, 3001))
     # no kernel for degenerate or scale-only calls
     assert sel(0, 4, 4, 1.0, FAKE, 4, FAKE, 4, FAKE, 4) == -1
     assert sel(4, 4, 4, 0.0, FAKE, 4, FAKE, 4, FAKE, 4) == -1
@@ -157,10 +158,10 @@ def test_force_config(sgemm_lib):
         assert not sgemm_lib.sgemm_config_name(
             sel(512, 512, 512, 1.0, FAKE, 512, FAKE, 512, FAKE, 512)).startswith("skinny")
         # a TMA configuration cannot take a misaligned operand: the table decides instead
-        tma_ids = [i for i in range(n) if "tma" in sgemm_lib.sgemm_config_name(i)]
+        tma_ids = [i for i in range(n) if sgemm_lib.sgemm_config_name(i).startswith(("dp_tma", "sk_tma"))]
         sgemm_lib.sgemm_force_config(tma_ids[0])
         got = sel(512, 512, 512, 1.0, FAKE + 4, 512, FAKE, 512, FAKE, 512)
-        assert "cpasync" in sgemm_lib.sgemm_config_name(got)
+        assert sgemm_lib.sgemm_config_name(got).startswith(("packed", "dp_cpasync", "sk_cpasync"))
         with pytest.raises(sgemm_lib.SgemmError):
             sgemm_lib.sgemm_force_config(n)
     finally:

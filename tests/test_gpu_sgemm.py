@@ -171,7 +171,8 @@ def test_each_config(sg, cfg, shape):
 
 
 @pytest.mark.parametrize("name", ["sk_tma_ws_128x256_s4", "sk_tma_ws_256x128_s4",
-                                  "sk_tma_ws_128x128_s3"])
+                                  "sk_tma_ws_128x128_s3", "sk_cpasync_128x256_s4",
+                                  "sk_cpasync_256x128_s4", "packed_sk_tma_128x256_s4"])
 def test_stream_k_deterministic_and_exact(sg, name):
     ids = {sg.sgemm_config_name(i): i for i in range(sg.sgemm_num_configs())}
     sg.sgemm_force_config(ids[name])
@@ -185,6 +186,9 @@ def test_stream_k_deterministic_and_exact(sg, name):
         got, ref = _check(Case(2304, 1792, 1000, 1.0, -1.0, "small_int", seed=12,
                                rows=sample_rows(2304)), sg)
         assert np.array_equal(got, ref)
+        # unaligned leading dimensions (cp.async loaders take them; TMA ones fall back)
+        _check(Case(4095, 3001, 1537, 0.7, -1.3, "normal", seed=13, rows=sample_rows(4095)), sg)
+        _check(Case(127, 129, 4099, 0.7, -1.3, "normal", seed=14), sg)
     finally:
         sg.sgemm_force_config(-1)
 
@@ -228,6 +232,36 @@ def test_strided_batched(sg, M, N, K, batch, cfg):
         _batched(sg, M, N, K, batch, M * K, K * N, M * N, 0.7, -1.3, sg.sgemm_strided_batched)
         _batched(sg, M, N, K, batch, M * K, K * N, M * N, 1.0, 1.0, sg.sgemm_strided_batched,
                  exact=True)
+    finally:
+        sg.sgemm_force_config(-1)
+
+
+@pytest.mark.parametrize("cfg", [-1, 14, 15])
+def test_strided_batched_unaligned(sg, cfg):
+    # odd leading dimensions and strides: repacked for TMA (or loaded with cp.async)
+    sg.sgemm_force_config(cfg)
+    try:
+        M, N, K, batch = 129, 131, 75, 3
+        import oracle
+        import synth
+        lda, ldb, ldc = K + 1, N + 3, N + 1
+        sA, sB, sC = M * lda + 5, K * ldb + 7, M * ldc + 1
+        A = synth.normal(1, sA * batch, 21).reshape(-1)
+        B = synth.normal(1, sB * batch, 22).reshape(-1)
+        C = synth.normal(1, sC * batch, 23).reshape(-1)
+        dA, dB, dC = (torch.from_numpy(x.copy()).cuda() for x in (A, B, C))
+        sg.sgemm_strided_batched(M, N, K, 0.7, dA, lda, sA, dB, ldb, sB, -1.3, dC, ldc, sC, batch)
+        assert sg.sgemm_device_status() == sg.SGEMM_OK
+        out = dC.cpu().numpy()
+        for b in range(batch):
+            a = np.ascontiguousarray(A[b * sA:b * sA + M * lda])
+            bb = np.ascontiguousarray(B[b * sB:b * sB + K * ldb])
+            c = np.ascontiguousarray(C[b * sC:b * sC + M * ldc])
+            ref = oracle.sgemm(M, N, K, 0.7, a, lda, bb, ldb, -1.3, c, ldc)
+            den = oracle.absdot(M, N, K, a, lda, bb, ldb)
+            got = out[b * sC:b * sC + M * ldc].reshape(M, ldc)[:, :N]
+            cin = c.reshape(M, ldc)[:, :N]
+            assert oracle.normalized_error(got, ref, den, 0.7, -1.3, cin) <= TOL
     finally:
         sg.sgemm_force_config(-1)
 
