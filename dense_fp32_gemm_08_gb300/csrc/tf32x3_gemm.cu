@@ -54,17 +54,31 @@ __device__ __forceinline__ void split_value(float x, float &big, float &small) {
 }
 
 // A (rows x cols, leading dimension lda, batch stride sA) -> big, small (rows x ldo each,
-// batch stride so), same orientation. Rows over the grid's y dimension, columns over threads.
+// batch stride so; ldo and so multiples of 4, outputs 16-byte aligned), same orientation.
+// Rows over the grid's y dimension, columns over threads; float4 access when A allows.
+template <bool VEC>
 __global__ void split_rows_kernel(const float *__restrict__ A, long long lda, long long sA,
                                   float *__restrict__ big, float *__restrict__ small,
                                   long long ldo, long long so, int rows, int cols, int batch) {
     const long long nrows = static_cast<long long>(rows) * batch;
+    const int stride = gridDim.x * blockDim.x;
     for (long long gr = blockIdx.y; gr < nrows; gr += gridDim.y) {
         const long long b = gr / rows, r = gr - b * rows;
         const float *src = A + b * sA + r * lda;
         float *hi = big + b * so + r * ldo;
         float *lo = small + b * so + r * ldo;
-        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x) {
+        const int c4 = VEC ? (cols & ~3) : 0;
+        for (int c = 4 * (blockIdx.x * blockDim.x + threadIdx.x); c < c4; c += 4 * stride) {
+            const float4 x = __ldcs(reinterpret_cast<const float4 *>(src + c));
+            float4 h, l;
+            split_value(x.x, h.x, l.x);
+            split_value(x.y, h.y, l.y);
+            split_value(x.z, h.z, l.z);
+            split_value(x.w, h.w, l.w);
+            *reinterpret_cast<float4 *>(hi + c) = h;
+            *reinterpret_cast<float4 *>(lo + c) = l;
+        }
+        for (int c = c4 + blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += stride) {
             float h, l;
             split_value(src[c], h, l);
             hi[c] = h;
@@ -73,34 +87,61 @@ __global__ void split_rows_kernel(const float *__restrict__ A, long long lda, lo
     }
 }
 
-// B (rows = K x cols = N, ldb, batch stride sB) -> transposed big, small (N x ldo, K
-// contiguous), through a 32 x 33 shared tile so that reads and writes are both coalesced.
-__global__ void split_transpose_kernel(const float *__restrict__ B, long long ldb, long long sB,
-                                       float *__restrict__ big, float *__restrict__ small,
-                                       long long ldo, long long so, int K, int N) {
-    __shared__ float tile_hi[32][33];
-    __shared__ float tile_lo[32][33];
+// B (K x N, ldb, batch stride sB) -> transposed big, small (N x ldo, K contiguous). A 32 x 32
+// tile goes through shared memory: 256 threads each read one float4 along n (when B allows)
+// and write one float4 along k of each output, so both sides move 16 bytes per thread.
+template <bool VEC>
+__global__ void __launch_bounds__(256)
+    split_transpose_kernel(const float *__restrict__ B, long long ldb, long long sB,
+                           float *__restrict__ big, float *__restrict__ small, long long ldo,
+                           long long so, int K, int N) {
+    __shared__ float tile[32][33];
     const int b = blockIdx.z;
     const int n0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
-    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    const int t = threadIdx.x;
     const float *Bb = B + b * sB;
-#pragma unroll
-    for (int j = 0; j < 32; j += 8) {
-        const int k = k0 + ty + j, n = n0 + tx;
-        float hi = 0.0f, lo = 0.0f;
-        if (k < K && n < N) split_value(Bb[static_cast<long long>(k) * ldb + n], hi, lo);
-        tile_hi[ty + j][tx] = hi;
-        tile_lo[ty + j][tx] = lo;
+    {
+        const int kr = t >> 3, nc = (t & 7) * 4;  // row k0 + kr, columns n0 + nc .. + 3
+        const int k = k0 + kr, n = n0 + nc;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (k < K) {
+            const float *src = Bb + static_cast<long long>(k) * ldb + n;
+            if (VEC && n + 3 < N) {
+                v = __ldcs(reinterpret_cast<const float4 *>(src));
+            } else {
+                if (n < N) v.x = src[0];
+                if (n + 1 < N) v.y = src[1];
+                if (n + 2 < N) v.z = src[2];
+                if (n + 3 < N) v.w = src[3];
+            }
+        }
+        tile[kr][nc] = v.x;
+        tile[kr][nc + 1] = v.y;
+        tile[kr][nc + 2] = v.z;
+        tile[kr][nc + 3] = v.w;
     }
     __syncthreads();
-    float *ob = big + b * so;
-    float *os = small + b * so;
-#pragma unroll
-    for (int j = 0; j < 32; j += 8) {
-        const int n = n0 + ty + j, k = k0 + tx;
-        if (n < N && k < K) {
-            ob[static_cast<long long>(n) * ldo + k] = tile_hi[tx][ty + j];
-            os[static_cast<long long>(n) * ldo + k] = tile_lo[tx][ty + j];
+    {
+        const int nr = t >> 3, kc = (t & 7) * 4;  // output row n0 + nr, k0 + kc .. + 3
+        const int n = n0 + nr, k = k0 + kc;
+        if (n < N) {
+            float4 h, l;
+            split_value(tile[kc][nr], h.x, l.x);
+            split_value(tile[kc + 1][nr], h.y, l.y);
+            split_value(tile[kc + 2][nr], h.z, l.z);
+            split_value(tile[kc + 3][nr], h.w, l.w);
+            float *ob = big + b * so + static_cast<long long>(n) * ldo + k;
+            float *os = small + b * so + static_cast<long long>(n) * ldo + k;
+            if (k + 3 < K) {
+                *reinterpret_cast<float4 *>(ob) = h;
+                *reinterpret_cast<float4 *>(os) = l;
+            } else {
+                const float hv[4] = {h.x, h.y, h.z, h.w}, lv[4] = {l.x, l.y, l.z, l.w};
+                for (int e = 0; e < 4 && k + e < K; ++e) {
+                    ob[e] = hv[e];
+                    os[e] = lv[e];
+                }
+            }
         }
     }
 }
@@ -451,18 +492,28 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
 
     {
         const long long nrows = static_cast<long long>(p.M) * p.batch;
-        const dim3 rgrid(static_cast<unsigned>(std::min<long long>((p.K + 255) / 256, 8)),
+        const bool vecA = aligned16(p.A) && p.lda % 4 == 0 && (p.batch <= 1 || p.strideA % 4 == 0);
+        const dim3 rgrid(static_cast<unsigned>(std::min<long long>((p.K + 1023) / 1024, 8)),
                          static_cast<unsigned>(std::min<long long>(nrows, 65535)));
-        split_rows_kernel<<<rgrid, 256, 0, stream>>>(p.A, p.lda, p.strideA, a_hi, a_lo, ldk,
-                                                     a_elems, p.M, p.K, p.batch);
+        if (vecA)
+            split_rows_kernel<true><<<rgrid, 256, 0, stream>>>(p.A, p.lda, p.strideA, a_hi, a_lo,
+                                                               ldk, a_elems, p.M, p.K, p.batch);
+        else
+            split_rows_kernel<false><<<rgrid, 256, 0, stream>>>(p.A, p.lda, p.strideA, a_hi, a_lo,
+                                                                ldk, a_elems, p.M, p.K, p.batch);
         err = cudaGetLastError();
         if (err != cudaSuccess) {
             *detail = "split kernel launch failed";
             return err;
         }
+        const bool vecB = aligned16(p.B) && p.ldb % 4 == 0 && (p.batch <= 1 || p.strideB % 4 == 0);
         dim3 grid((p.N + 31) / 32, (p.K + 31) / 32, p.batch);
-        split_transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(p.B, p.ldb, p.strideB, b_hi, b_lo,
-                                                               ldk, b_elems, p.K, p.N);
+        if (vecB)
+            split_transpose_kernel<true><<<grid, 256, 0, stream>>>(p.B, p.ldb, p.strideB, b_hi,
+                                                                   b_lo, ldk, b_elems, p.K, p.N);
+        else
+            split_transpose_kernel<false><<<grid, 256, 0, stream>>>(p.B, p.ldb, p.strideB, b_hi,
+                                                                    b_lo, ldk, b_elems, p.K, p.N);
         err = cudaGetLastError();
         if (err != cudaSuccess) {
             *detail = "split-transpose kernel launch failed";
