@@ -5,7 +5,7 @@ beta = 0 (the pages' headline problem, 137.4 GFLOP per call). A "step" is one li
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload headline|sq256|edge0..edge3|sweepNNNN|llm_qkv|llm_up|llm_down|llm_head]
-                  [--path simt|3xtf32]
+                  [--path simt|3xtf32|tf32]
 
 Timing: W untimed warm-up steps, then K steps. Before every step a 256 MiB buffer is written
 (L2 is 129 MB) so each step starts with cold L2; each step's GEMM is bracketed by CUDA
@@ -273,7 +273,7 @@ def run_ours(args):
     w = WORKLOADS[args.workload]
     M, N, K, alpha, beta = w["M"], w["N"], w["K"], w["alpha"], w["beta"]
     flops = 2.0 * M * N * K
-    entry = sg.sgemm_3xtf32 if args.path == "3xtf32" else sg.sgemm
+    entry = {"simt": sg.sgemm, "3xtf32": sg.sgemm_3xtf32, "tf32": sg.sgemm_tf32}[args.path]
 
     A_h, B_h, C_h = host_inputs(w)
     A = torch.from_numpy(A_h).to(dev)
@@ -283,7 +283,8 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     cfg_id = sg.sgemm_select_config(M, N, K, alpha, A, K, B, N, C, N)
-    kernel = sg.sgemm_config_name(cfg_id) if args.path == "simt" else "tf32x3_tcgen05"
+    kernel = (sg.sgemm_config_name(cfg_id) if args.path == "simt"
+              else {"3xtf32": "tf32x3_tcgen05", "tf32": "tf32_tcgen05"}[args.path])
 
     def step():
         entry(M, N, K, alpha, A, K, B, N, beta, C, N, stream)
@@ -334,6 +335,7 @@ def run_ours(args):
             roof["frac_at_run_clock"] = round(
                 achieved_tflops / (sms * clk["sm_mhz"] * 1e6 * FMA_PER_CLK_PER_SM * 2 / 1e12), 4)
     else:
+        products = 3 if args.path == "3xtf32" else 1
         peaks = measured_peaks()
         if peaks.get("bf16_tflops"):
             tf32_peak = peaks["bf16_tflops"] * TF32_NOMINAL_TFLOPS / BF16_NOMINAL_TFLOPS
@@ -345,11 +347,11 @@ def run_ours(args):
         roof = {"bound": "tensor", "achieved": round(achieved_tflops, 3),
                 "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved_tflops / tf32_peak, 4),
-                "issued_tflops": round(3 * achieved_tflops, 3),
-                "issued_frac": round(3 * achieved_tflops / tf32_peak, 4),
+                "issued_tflops": round(products * achieved_tflops, 3),
+                "issued_frac": round(products * achieved_tflops / tf32_peak, 4),
                 "traffic": ncu_traffic(kernel, args.workload, "3xtf32"),
-                "peak_basis": basis + "; achieved counts 2MNK, issued counts the 3 TF32 "
-                                      "products per multiply-add",
+                "peak_basis": basis + f"; achieved counts 2MNK, issued counts the {products} "
+                                      "TF32 product(s) per multiply-add",
                 "frac_of_fp32_simt_peak": round(achieved_tflops / peak_boost, 4)}
 
     e2e = None
@@ -482,7 +484,7 @@ def parse(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="headline")
-    ap.add_argument("--path", choices=["simt", "3xtf32"], default="simt")
+    ap.add_argument("--path", choices=["simt", "3xtf32", "tf32"], default="simt")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")

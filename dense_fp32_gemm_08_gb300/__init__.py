@@ -16,7 +16,7 @@ from pathlib import Path
 
 __all__ = [
     "SgemmError", "library_path", "lib", "sgemm", "sgemm_strided_batched", "sgemm_3xtf32",
-    "sgemm_3xtf32_strided_batched", "sgemm_noalloc", "sgemm_status_string", "sgemm_last_error",
+    "sgemm_3xtf32_strided_batched", "sgemm_tf32", "sgemm_tf32_strided_batched", "sgemm_noalloc", "sgemm_status_string", "sgemm_last_error",
     "sgemm_device_status", "sgemm_release_workspace", "sgemm_num_configs",
     "sgemm_config_name", "sgemm_select_config", "sgemm_force_config",
     "sgemm_selftest_bounded_wait", "matmul",
@@ -60,8 +60,9 @@ def _bind(L):
     gemm = [i64, i64, i64, f32, p, i64, p, i64, f32, p, i64, p]
     batched = [i64, i64, i64, f32, p, i64, i64, p, i64, i64, f32, p, i64, i64, i64, p]
     for name, args in (("sgemm", gemm), ("sgemm_3xtf32", gemm), ("sgemm_noalloc", gemm),
-                       ("sgemm_strided_batched", batched),
-                       ("sgemm_3xtf32_strided_batched", batched)):
+                       ("sgemm_tf32", gemm), ("sgemm_strided_batched", batched),
+                       ("sgemm_3xtf32_strided_batched", batched),
+                       ("sgemm_tf32_strided_batched", batched)):
         fn = getattr(L, name)
         fn.argtypes = args
         fn.restype = i32
@@ -147,6 +148,19 @@ def sgemm_3xtf32_strided_batched(M, N, K, alpha, A, lda, strideA, B, ldb, stride
     _check(lib().sgemm_3xtf32_strided_batched(M, N, K, alpha, _ptr(A), lda, strideA, _ptr(B),
                                               ldb, strideB, beta, _ptr(C), ldc, strideC, batch,
                                               _stream(stream)))
+
+
+def sgemm_tf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:
+    """One TF32 product per multiply-add: faster, TF32 accuracy (see include/sgemm.h)."""
+    _check(lib().sgemm_tf32(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
+                            _stream(stream)))
+
+
+def sgemm_tf32_strided_batched(M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+                               strideC, batch, stream=None) -> None:
+    _check(lib().sgemm_tf32_strided_batched(M, N, K, alpha, _ptr(A), lda, strideA, _ptr(B), ldb,
+                                            strideB, beta, _ptr(C), ldc, strideC, batch,
+                                            _stream(stream)))
 
 
 def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:

@@ -155,12 +155,15 @@ sgemm_status_t run_simt(const Args &a, cudaStream_t stream) {
     return SGEMM_OK;
 }
 
-sgemm_status_t run_tf32x3(const Args &a, cudaStream_t stream) {
+enum Path { kPathSimt, kPathTf32x3, kPathTf32 };
+
+sgemm_status_t run_tensor(const Args &a, cudaStream_t stream, Path path) {
     const sg::SimtProblem p = to_problem(a);
     if (!sg::tf32x3_supports(p))
-        return fail(SGEMM_ERR_UNSUPPORTED, "3xTF32 path takes at most 65535 batch entries");
+        return fail(SGEMM_ERR_UNSUPPORTED, "the TF32 paths take at most 65535 batch entries");
     const char *detail = "";
-    cudaError_t err = sg::tf32x3_launch(p, stream, &detail);
+    cudaError_t err = path == kPathTf32 ? sg::tf32_launch(p, stream, &detail)
+                                        : sg::tf32x3_launch(p, stream, &detail);
     if (err != cudaSuccess) return fail_cuda(detail, err);
     return SGEMM_OK;
 }
@@ -170,7 +173,7 @@ bool have_device() {
     return cudaGetDevice(&dev) == cudaSuccess;
 }
 
-sgemm_status_t dispatch(const Args &a, void *stream_ptr, bool tensor_path) {
+sgemm_status_t dispatch(const Args &a, void *stream_ptr, Path path) {
     t_last_error[0] = '\0';
     sgemm_status_t st = validate(a);
     if (st != SGEMM_OK) return st;
@@ -180,7 +183,7 @@ sgemm_status_t dispatch(const Args &a, void *stream_ptr, bool tensor_path) {
     if (!have_device()) return fail(SGEMM_ERR_UNSUPPORTED, "no CUDA device available");
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     if (a.alpha == 0.0f || a.K == 0) return run_scale(a, stream);
-    return tensor_path ? run_tf32x3(a, stream) : run_simt(a, stream);
+    return path == kPathSimt ? run_simt(a, stream) : run_tensor(a, stream, path);
 }
 
 }  // namespace
@@ -191,7 +194,7 @@ sgemm_status_t sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float *
                      const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
                      void *stream) {
     Args a{M, N, K, alpha, beta, A, lda, 0, B, ldb, 0, C, ldc, 0, 1};
-    return dispatch(a, stream, false);
+    return dispatch(a, stream, kPathSimt);
 }
 
 sgemm_status_t sgemm_strided_batched(int64_t M, int64_t N, int64_t K, float alpha,
@@ -200,14 +203,14 @@ sgemm_status_t sgemm_strided_batched(int64_t M, int64_t N, int64_t K, float alph
                                      float *C, int64_t ldc, int64_t strideC, int64_t batch,
                                      void *stream) {
     Args a{M, N, K, alpha, beta, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch};
-    return dispatch(a, stream, false);
+    return dispatch(a, stream, kPathSimt);
 }
 
 sgemm_status_t sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                             int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                             int64_t ldc, void *stream) {
     Args a{M, N, K, alpha, beta, A, lda, 0, B, ldb, 0, C, ldc, 0, 1};
-    return dispatch(a, stream, true);
+    return dispatch(a, stream, kPathTf32x3);
 }
 
 sgemm_status_t sgemm_3xtf32_strided_batched(int64_t M, int64_t N, int64_t K, float alpha,
@@ -216,7 +219,23 @@ sgemm_status_t sgemm_3xtf32_strided_batched(int64_t M, int64_t N, int64_t K, flo
                                             float beta, float *C, int64_t ldc, int64_t strideC,
                                             int64_t batch, void *stream) {
     Args a{M, N, K, alpha, beta, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch};
-    return dispatch(a, stream, true);
+    return dispatch(a, stream, kPathTf32x3);
+}
+
+sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                          int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                          int64_t ldc, void *stream) {
+    Args a{M, N, K, alpha, beta, A, lda, 0, B, ldb, 0, C, ldc, 0, 1};
+    return dispatch(a, stream, kPathTf32);
+}
+
+sgemm_status_t sgemm_tf32_strided_batched(int64_t M, int64_t N, int64_t K, float alpha,
+                                          const float *A, int64_t lda, int64_t strideA,
+                                          const float *B, int64_t ldb, int64_t strideB,
+                                          float beta, float *C, int64_t ldc, int64_t strideC,
+                                          int64_t batch, void *stream) {
+    Args a{M, N, K, alpha, beta, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch};
+    return dispatch(a, stream, kPathTf32);
 }
 
 sgemm_status_t sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const float *A,

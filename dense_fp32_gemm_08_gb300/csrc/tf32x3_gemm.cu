@@ -26,6 +26,11 @@
 // over interleaved k-blocks cut it by about sqrt(ACCS).
 // Every wait is bounded; a wait that expires raises the fault word, and the CTA still meets at
 // the final barrier and frees its TMEM.
+//
+// Single-product mode (PRODUCTS = 1, the "1xTF32" fast path): the pre-pass writes only the big
+// parts (tf32_rna of each value) and the kernel issues big_A.big_B alone, with twice the
+// stages in the same shared memory. Each product is then off by at most (2u + u^2)|a b|,
+// u = 2^-11, so the result carries TF32 rather than fp32 accuracy.
 #include "ptx.cuh"
 #include "tf32x3_gemm.cuh"
 
@@ -56,7 +61,7 @@ __device__ __forceinline__ void split_value(float x, float &big, float &small) {
 // A (rows x cols, leading dimension lda, batch stride sA) -> big, small (rows x ldo each,
 // batch stride so; ldo and so multiples of 4, outputs 16-byte aligned), same orientation.
 // Rows over the grid's y dimension, columns over threads; float4 access when A allows.
-template <bool VEC>
+template <bool VEC, bool SMALL>
 __global__ void split_rows_kernel(const float *__restrict__ A, long long lda, long long sA,
                                   float *__restrict__ big, float *__restrict__ small,
                                   long long ldo, long long so, int rows, int cols, int batch) {
@@ -76,13 +81,13 @@ __global__ void split_rows_kernel(const float *__restrict__ A, long long lda, lo
             split_value(x.z, h.z, l.z);
             split_value(x.w, h.w, l.w);
             *reinterpret_cast<float4 *>(hi + c) = h;
-            *reinterpret_cast<float4 *>(lo + c) = l;
+            if (SMALL) *reinterpret_cast<float4 *>(lo + c) = l;
         }
         for (int c = c4 + blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += stride) {
             float h, l;
             split_value(src[c], h, l);
             hi[c] = h;
-            lo[c] = l;
+            if (SMALL) lo[c] = l;
         }
     }
 }
@@ -90,7 +95,7 @@ __global__ void split_rows_kernel(const float *__restrict__ A, long long lda, lo
 // B (K x N, ldb, batch stride sB) -> transposed big, small (N x ldo, K contiguous). A 32 x 32
 // tile goes through shared memory: 256 threads each read one float4 along n (when B allows)
 // and write one float4 along k of each output, so both sides move 16 bytes per thread.
-template <bool VEC>
+template <bool VEC, bool SMALL>
 __global__ void __launch_bounds__(256)
     split_transpose_kernel(const float *__restrict__ B, long long ldb, long long sB,
                            float *__restrict__ big, float *__restrict__ small, long long ldo,
@@ -134,12 +139,12 @@ __global__ void __launch_bounds__(256)
             float *os = small + b * so + static_cast<long long>(n) * ldo + k;
             if (k + 3 < K) {
                 *reinterpret_cast<float4 *>(ob) = h;
-                *reinterpret_cast<float4 *>(os) = l;
+                if (SMALL) *reinterpret_cast<float4 *>(os) = l;
             } else {
                 const float hv[4] = {h.x, h.y, h.z, h.w}, lv[4] = {l.x, l.y, l.z, l.w};
                 for (int e = 0; e < 4 && k + e < K; ++e) {
                     ob[e] = hv[e];
-                    os[e] = lv[e];
+                    if (SMALL) os[e] = lv[e];
                 }
             }
         }
@@ -220,7 +225,7 @@ struct TParams {
     int c_vec4;
 };
 
-template <int BN, int STAGES, int ACCS>
+template <int BN, int STAGES, int ACCS, int PRODUCTS>
 __global__ void __launch_bounds__(192, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap mapAhi,
                        const __grid_constant__ CUtensorMap mapAlo,
@@ -228,7 +233,9 @@ __global__ void __launch_bounds__(192, 1)
                        const __grid_constant__ CUtensorMap mapBlo, const TParams p) {
     constexpr uint32_t A_BYTES = BM * BK * 4;  // 16 KiB per part
     constexpr uint32_t B_BYTES = BN * BK * 4;
-    constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
+    static_assert(PRODUCTS == 3 || PRODUCTS == 1, "3xTF32 or a single TF32 product");
+    constexpr uint32_t PARTS = PRODUCTS == 3 ? 2 : 1;  // big (and small) of each operand
+    constexpr uint32_t STAGE_BYTES = PARTS * (A_BYTES + B_BYTES);
     constexpr uint32_t IDESC = idesc_tf32(BN);
     constexpr uint32_t TMEM_COLS = BN * ACCS;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
@@ -282,9 +289,11 @@ __global__ void __launch_bounds__(192, 1)
             uint8_t *st = smem + s * STAGE_BYTES;
             mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
             tma_load_3d(st, &mapAhi, &full[s], kb * BK, m0, b);
-            tma_load_3d(st + A_BYTES, &mapAlo, &full[s], kb * BK, m0, b);
-            tma_load_3d(st + 2 * A_BYTES, &mapBhi, &full[s], kb * BK, n0, b);
-            tma_load_3d(st + 2 * A_BYTES + B_BYTES, &mapBlo, &full[s], kb * BK, n0, b);
+            tma_load_3d(st + PARTS * A_BYTES, &mapBhi, &full[s], kb * BK, n0, b);
+            if (PRODUCTS == 3) {
+                tma_load_3d(st + A_BYTES, &mapAlo, &full[s], kb * BK, m0, b);
+                tma_load_3d(st + 2 * A_BYTES + B_BYTES, &mapBlo, &full[s], kb * BK, n0, b);
+            }
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer ----
@@ -298,15 +307,19 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after();
             const uint32_t st = smem_addr(smem + s * STAGE_BYTES);
             const uint32_t a_hi = st, a_lo = st + A_BYTES;
-            const uint32_t b_hi = st + 2 * A_BYTES, b_lo = b_hi + B_BYTES;
+            const uint32_t b_hi = st + PARTS * A_BYTES, b_lo = b_hi + B_BYTES;
             const uint32_t d = tmem + static_cast<uint32_t>((kb % ACCS) * BN);
 #pragma unroll
             for (int kk = 0; kk < BK / 8; ++kk) {
                 const uint32_t off = kk * 32;  // 8 tf32 values along k
                 const uint32_t acc0 = (kb >= ACCS || kk > 0) ? 1u : 0u;  // first write: overwrite
-                mma_tf32(d, smem_desc_sw128(a_lo + off), smem_desc_sw128(b_hi + off), IDESC, acc0);
-                mma_tf32(d, smem_desc_sw128(a_hi + off), smem_desc_sw128(b_lo + off), IDESC, 1u);
-                mma_tf32(d, smem_desc_sw128(a_hi + off), smem_desc_sw128(b_hi + off), IDESC, 1u);
+                if (PRODUCTS == 3) {
+                    mma_tf32(d, smem_desc_sw128(a_lo + off), smem_desc_sw128(b_hi + off), IDESC, acc0);
+                    mma_tf32(d, smem_desc_sw128(a_hi + off), smem_desc_sw128(b_lo + off), IDESC, 1u);
+                    mma_tf32(d, smem_desc_sw128(a_hi + off), smem_desc_sw128(b_hi + off), IDESC, 1u);
+                } else {
+                    mma_tf32(d, smem_desc_sw128(a_hi + off), smem_desc_sw128(b_hi + off), IDESC, acc0);
+                }
             }
             mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
@@ -450,11 +463,12 @@ bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u
 
 constexpr int kMaxDevices = 64;
 
-template <int BN, int STAGES, int ACCS>
+template <int BN, int STAGES, int ACCS, int PRODUCTS>
 cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char **detail) {
-    constexpr size_t STAGE_BYTES = 2 * BM * BK * 4 + 2 * static_cast<size_t>(BN) * BK * 4;
+    constexpr size_t PARTS = PRODUCTS == 3 ? 2 : 1;
+    constexpr size_t STAGE_BYTES = PARTS * (BM * BK * 4 + static_cast<size_t>(BN) * BK * 4);
     constexpr size_t SMEM = STAGES * STAGE_BYTES + (2 * STAGES + 1) * 8 + 16 + 1024;
-    auto kernel = tf32x3_gemm_kernel<BN, STAGES, ACCS>;
+    auto kernel = tf32x3_gemm_kernel<BN, STAGES, ACCS, PRODUCTS>;
 
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -478,7 +492,7 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
     const long long ldk = (static_cast<long long>(p.K) + 3) / 4 * 4;
     const long long a_elems = static_cast<long long>(p.M) * ldk;
     const long long b_elems = static_cast<long long>(p.N) * ldk;
-    const long long per_batch = 2 * a_elems + 2 * b_elems;
+    const long long per_batch = static_cast<long long>(PARTS) * (a_elems + b_elems);
     float *ws = nullptr;
     err = split_workspace(dev, stream, static_cast<size_t>(per_batch) * p.batch * 4, &ws);
     if (err != cudaSuccess) {
@@ -486,9 +500,10 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
         return err;
     }
     float *a_hi = ws;
-    float *a_lo = a_hi + a_elems * p.batch;
+    float *a_lo = PARTS == 2 ? a_hi + a_elems * p.batch : a_hi;
     float *b_hi = a_lo + a_elems * p.batch;
-    float *b_lo = b_hi + b_elems * p.batch;
+    float *b_lo = PARTS == 2 ? b_hi + b_elems * p.batch : b_hi;
+    constexpr bool SMALL = PARTS == 2;
 
     {
         const long long nrows = static_cast<long long>(p.M) * p.batch;
@@ -496,11 +511,11 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
         const dim3 rgrid(static_cast<unsigned>(std::min<long long>((p.K + 1023) / 1024, 8)),
                          static_cast<unsigned>(std::min<long long>(nrows, 65535)));
         if (vecA)
-            split_rows_kernel<true><<<rgrid, 256, 0, stream>>>(p.A, p.lda, p.strideA, a_hi, a_lo,
-                                                               ldk, a_elems, p.M, p.K, p.batch);
+            split_rows_kernel<true, SMALL><<<rgrid, 256, 0, stream>>>(
+                p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.M, p.K, p.batch);
         else
-            split_rows_kernel<false><<<rgrid, 256, 0, stream>>>(p.A, p.lda, p.strideA, a_hi, a_lo,
-                                                                ldk, a_elems, p.M, p.K, p.batch);
+            split_rows_kernel<false, SMALL><<<rgrid, 256, 0, stream>>>(
+                p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.M, p.K, p.batch);
         err = cudaGetLastError();
         if (err != cudaSuccess) {
             *detail = "split kernel launch failed";
@@ -509,11 +524,11 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
         const bool vecB = aligned16(p.B) && p.ldb % 4 == 0 && (p.batch <= 1 || p.strideB % 4 == 0);
         dim3 grid((p.N + 31) / 32, (p.K + 31) / 32, p.batch);
         if (vecB)
-            split_transpose_kernel<true><<<grid, 256, 0, stream>>>(p.B, p.ldb, p.strideB, b_hi,
-                                                                   b_lo, ldk, b_elems, p.K, p.N);
+            split_transpose_kernel<true, SMALL><<<grid, 256, 0, stream>>>(
+                p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.K, p.N);
         else
-            split_transpose_kernel<false><<<grid, 256, 0, stream>>>(p.B, p.ldb, p.strideB, b_hi,
-                                                                    b_lo, ldk, b_elems, p.K, p.N);
+            split_transpose_kernel<false, SMALL><<<grid, 256, 0, stream>>>(
+                p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.K, p.N);
         err = cudaGetLastError();
         if (err != cudaSuccess) {
             *detail = "split-transpose kernel launch failed";
@@ -559,7 +574,11 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
 bool tf32x3_supports(const SimtProblem &p) { return p.batch <= 65535; }
 
 cudaError_t tf32x3_launch(const SimtProblem &p, cudaStream_t stream, const char **detail) {
-    return launch_tf32x3<128, 3, 4>(p, stream, detail);
+    return launch_tf32x3<128, 3, 4, 3>(p, stream, detail);
+}
+
+cudaError_t tf32_launch(const SimtProblem &p, cudaStream_t stream, const char **detail) {
+    return launch_tf32x3<128, 6, 4, 1>(p, stream, detail);
 }
 
 cudaError_t tf32x3_release_workspaces() {

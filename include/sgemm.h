@@ -108,6 +108,27 @@ sgemm_status_t sgemm_3xtf32_strided_batched(int64_t M, int64_t N, int64_t K, flo
                                             int64_t strideC, int64_t batch, void *stream);
 
 /*
+ * The fast, lower-accuracy tensor-core mode: each operand value is rounded to TF32
+ * (tf32_rna, 10 explicit mantissa bits) and one TF32 product per multiply-add accumulates in
+ * fp32 tensor memory. The pages quote the TF32 tensor rate at twice the FP32 rate ("GEMM
+ * scrapbook", closing remarks). Accuracy: each product is off by at most (2u + u^2)|a b| with
+ * u = 2^-11, so the normalised error is bounded by about 9.8e-4 (plus fp32 accumulation),
+ * not by the fp32 bound of the other entry points. Same arguments, errors and conventions as
+ * sgemm(), any alignment; the rounded operands live in the same kind of per-(device, stream)
+ * workspace as the 3xTF32 path (half its size).
+ */
+sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, float alpha,
+                          const float *A, int64_t lda, const float *B, int64_t ldb,
+                          float beta, float *C, int64_t ldc, void *stream);
+
+/* Batched form of sgemm_tf32; the arguments are those of sgemm_strided_batched. */
+sgemm_status_t sgemm_tf32_strided_batched(int64_t M, int64_t N, int64_t K, float alpha,
+                                          const float *A, int64_t lda, int64_t strideA,
+                                          const float *B, int64_t ldb, int64_t strideB,
+                                          float beta, float *C, int64_t ldc,
+                                          int64_t strideC, int64_t batch, void *stream);
+
+/*
  * The same product as sgemm(), for callers that must not have the library allocate device
  * memory: an application that hands its whole memory budget to its own pool, so that a
  * cudaMalloc from a library would fail or fragment that pool; or code that cannot afford
