@@ -16,7 +16,8 @@ from pathlib import Path
 
 __all__ = [
     "SgemmError", "library_path", "lib", "sgemm", "sgemm_strided_batched", "sgemm_3xtf32",
-    "sgemm_3xtf32_strided_batched", "sgemm_tf32", "sgemm_tf32_strided_batched", "sgemm_noalloc", "sgemm_status_string", "sgemm_last_error",
+    "sgemm_3xtf32_strided_batched", "sgemm_tf32", "sgemm_tf32_strided_batched", "sgemm_ex",
+    "sgemm_ex_strided_batched", "sgemm_noalloc", "sgemm_status_string", "sgemm_last_error",
     "sgemm_device_status", "sgemm_release_workspace", "sgemm_num_configs",
     "sgemm_config_name", "sgemm_select_config", "sgemm_force_config",
     "sgemm_selftest_bounded_wait", "matmul",
@@ -29,6 +30,10 @@ SGEMM_ERR_INVALID_VALUE = 1
 SGEMM_ERR_LAUNCH = 2
 SGEMM_ERR_TIMEOUT = 3
 SGEMM_ERR_UNSUPPORTED = 4
+
+SGEMM_OP_N, SGEMM_OP_T = 0, 1
+SGEMM_PATH_SIMT, SGEMM_PATH_3XTF32, SGEMM_PATH_TF32 = 0, 1, 2
+_PATHS = {"simt": SGEMM_PATH_SIMT, "3xtf32": SGEMM_PATH_3XTF32, "tf32": SGEMM_PATH_TF32}
 
 _LIBRARY = Path(__file__).resolve().with_name("libsgemm_gb300.so")
 _lib = None
@@ -66,6 +71,10 @@ def _bind(L):
         fn = getattr(L, name)
         fn.argtypes = args
         fn.restype = i32
+    L.sgemm_ex.argtypes = [i32, i32, i32] + gemm
+    L.sgemm_ex.restype = i32
+    L.sgemm_ex_strided_batched.argtypes = [i32, i32, i32] + batched
+    L.sgemm_ex_strided_batched.restype = i32
     L.sgemm_status_string.argtypes = [i32]
     L.sgemm_status_string.restype = ctypes.c_char_p
     L.sgemm_last_error.argtypes = []
@@ -161,6 +170,31 @@ def sgemm_tf32_strided_batched(M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
     _check(lib().sgemm_tf32_strided_batched(M, N, K, alpha, _ptr(A), lda, strideA, _ptr(B), ldb,
                                             strideB, beta, _ptr(C), ldc, strideC, batch,
                                             _stream(stream)))
+
+
+def _op(t) -> int:
+    if t in (0, 1):
+        return int(t)
+    if isinstance(t, str) and t.upper() in ("N", "T"):
+        return SGEMM_OP_T if t.upper() == "T" else SGEMM_OP_N
+    return int(bool(t))
+
+
+def sgemm_ex(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, path="simt",
+             stream=None) -> None:
+    """C = alpha * op(A) op(B) + beta * C; transa / transb are 'N' / 'T' (or 0 / 1),
+    path is 'simt', '3xtf32' or 'tf32' (or its enum value)."""
+    pth = _PATHS.get(path, path) if isinstance(path, str) else int(path)
+    _check(lib().sgemm_ex(_op(transa), _op(transb), pth, M, N, K, alpha, _ptr(A), lda, _ptr(B),
+                          ldb, beta, _ptr(C), ldc, _stream(stream)))
+
+
+def sgemm_ex_strided_batched(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
+                             beta, C, ldc, strideC, batch, path="simt", stream=None) -> None:
+    pth = _PATHS.get(path, path) if isinstance(path, str) else int(path)
+    _check(lib().sgemm_ex_strided_batched(_op(transa), _op(transb), pth, M, N, K, alpha, _ptr(A),
+                                          lda, strideA, _ptr(B), ldb, strideB, beta, _ptr(C), ldc,
+                                          strideC, batch, _stream(stream)))
 
 
 def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:

@@ -79,14 +79,18 @@ struct Args {
     float *C;
     long long ldc, sC;
     long long batch;
+    bool ta = false, tb = false;  // A stored K x M, B stored N x K
 };
 
 // Checks shared by every entry point. Returns SGEMM_OK when the arguments are valid.
 sgemm_status_t validate(const Args &a) {
     if (a.M < 0 || a.N < 0 || a.K < 0) return fail(SGEMM_ERR_INVALID_VALUE, "M, N and K must be >= 0");
     if (a.batch < 0) return fail(SGEMM_ERR_INVALID_VALUE, "batch must be >= 0");
-    if (a.lda < (a.K > 1 ? a.K : 1)) return fail(SGEMM_ERR_INVALID_VALUE, "lda < max(1, K)");
-    if (a.ldb < (a.N > 1 ? a.N : 1)) return fail(SGEMM_ERR_INVALID_VALUE, "ldb < max(1, N)");
+    const long long acols = a.ta ? a.M : a.K, bcols = a.tb ? a.K : a.N;
+    if (a.lda < (acols > 1 ? acols : 1))
+        return fail(SGEMM_ERR_INVALID_VALUE, a.ta ? "lda < max(1, M) (A transposed)" : "lda < max(1, K)");
+    if (a.ldb < (bcols > 1 ? bcols : 1))
+        return fail(SGEMM_ERR_INVALID_VALUE, a.tb ? "ldb < max(1, K) (B transposed)" : "ldb < max(1, N)");
     if (a.ldc < (a.N > 1 ? a.N : 1)) return fail(SGEMM_ERR_INVALID_VALUE, "ldc < max(1, N)");
     if (a.sA < 0 || a.sB < 0 || a.sC < 0)
         return fail(SGEMM_ERR_INVALID_VALUE, "batch strides must be >= 0");
@@ -134,6 +138,8 @@ sg::SimtProblem to_problem(const Args &a) {
     p.strideB = a.batch > 1 ? a.sB : 0;
     p.strideC = a.batch > 1 ? a.sC : 0;
     p.batch = static_cast<int>(a.batch);
+    p.transA = a.ta;
+    p.transB = a.tb;
     return p;
 }
 
@@ -144,7 +150,14 @@ int choose_simt(const sg::SimtProblem &p) {
 }
 
 sgemm_status_t run_simt(const Args &a, cudaStream_t stream) {
-    const sg::SimtProblem p = to_problem(a);
+    sg::SimtProblem p = to_problem(a);
+    if (p.transA || p.transB) {  // the tile kernels read op(A), op(B) row-major
+        const char *detail = "";
+        sg::SimtProblem q;
+        cudaError_t err = sg::simt_untranspose(p, stream, &q, &detail);
+        if (err != cudaSuccess) return fail_cuda(detail, err);
+        p = q;
+    }
     const int id = choose_simt(p);
     if (log_enabled())
         std::fprintf(stderr, "[sgemm] M=%lld N=%lld K=%lld batch=%lld -> %s\n", a.M, a.N, a.K,
@@ -265,6 +278,37 @@ sgemm_status_t sgemm_selftest_bounded_wait(int which, void *stream_ptr) {
     cudaError_t err = sg::simt_selftest_wait(which, static_cast<cudaStream_t>(stream_ptr));
     if (err != cudaSuccess) return fail_cuda("self-test kernel launch", err);
     return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_ex_strided_batched(sgemm_op_t transa, sgemm_op_t transb, sgemm_path_t path,
+                                        int64_t M, int64_t N, int64_t K, float alpha,
+                                        const float *A, int64_t lda, int64_t strideA,
+                                        const float *B, int64_t ldb, int64_t strideB, float beta,
+                                        float *C, int64_t ldc, int64_t strideC, int64_t batch,
+                                        void *stream) {
+    t_last_error[0] = '\0';
+    if ((transa != SGEMM_OP_N && transa != SGEMM_OP_T) ||
+        (transb != SGEMM_OP_N && transb != SGEMM_OP_T))
+        return fail(SGEMM_ERR_INVALID_VALUE, "transa and transb must be SGEMM_OP_N or SGEMM_OP_T");
+    Path pth;
+    switch (path) {
+        case SGEMM_PATH_SIMT: pth = kPathSimt; break;
+        case SGEMM_PATH_3XTF32: pth = kPathTf32x3; break;
+        case SGEMM_PATH_TF32: pth = kPathTf32; break;
+        default: return fail(SGEMM_ERR_INVALID_VALUE, "unknown path");
+    }
+    Args a{M, N, K, alpha, beta, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch};
+    a.ta = transa == SGEMM_OP_T;
+    a.tb = transb == SGEMM_OP_T;
+    return dispatch(a, stream, pth);
+}
+
+sgemm_status_t sgemm_ex(sgemm_op_t transa, sgemm_op_t transb, sgemm_path_t path, int64_t M,
+                        int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                        const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                        void *stream) {
+    return sgemm_ex_strided_batched(transa, transb, path, M, N, K, alpha, A, lda, 0, B, ldb, 0,
+                                    beta, C, ldc, 0, 1, stream);
 }
 
 const char *sgemm_status_string(sgemm_status_t status) {

@@ -1245,17 +1245,21 @@ dim3 rows_grid(long long rows, int cols) {
 struct PackWorkspace {
     int dev;
     cudaStream_t stream;
+    int slot;  // 0: transposed copies, 1: realigned copies (both may live at once)
     void *ptr;
     size_t bytes;
 };
 std::mutex g_pack_mutex;
 std::vector<PackWorkspace> g_pack_ws;
 
-cudaError_t pack_workspace(int dev, cudaStream_t stream, size_t bytes, float **out) {
+constexpr int kSlotTransposed = 0;
+constexpr int kSlotRealigned = 1;
+
+cudaError_t pack_workspace(int dev, cudaStream_t stream, int slot, size_t bytes, float **out) {
     std::lock_guard<std::mutex> lock(g_pack_mutex);
     PackWorkspace *e = nullptr;
     for (auto &w : g_pack_ws)
-        if (w.dev == dev && w.stream == stream) e = &w;
+        if (w.dev == dev && w.stream == stream && w.slot == slot) e = &w;
     if (e && e->bytes < bytes) {
         cudaError_t err = cudaFree(e->ptr);
         e->ptr = nullptr;
@@ -1263,7 +1267,7 @@ cudaError_t pack_workspace(int dev, cudaStream_t stream, size_t bytes, float **o
         if (err != cudaSuccess) return err;
     }
     if (!e) {
-        g_pack_ws.push_back({dev, stream, nullptr, 0});
+        g_pack_ws.push_back({dev, stream, slot, nullptr, 0});
         e = &g_pack_ws.back();
     }
     if (!e->ptr) {
@@ -1300,7 +1304,8 @@ cudaError_t launch_packed(int inner, const SimtProblem &p, cudaStream_t stream,
             return err;
         }
         float *ws = nullptr;
-        err = pack_workspace(dev, stream, static_cast<size_t>(elemsA + elemsB) * p.batch * 4, &ws);
+        err = pack_workspace(dev, stream, kSlotRealigned,
+                             static_cast<size_t>(elemsA + elemsB) * p.batch * 4, &ws);
         if (err != cudaSuccess) {
             *detail = "repacking workspace allocation failed";
             return err;
@@ -1351,6 +1356,84 @@ cudaError_t release_pack_workspaces() {
     cudaSetDevice(cur);
     g_pack_ws.clear();
     return first;
+}
+
+// ---- transposed operands -------------------------------------------------------------------------
+namespace {
+
+// src (rows x cols, leading dimension lds, batch stride ss) -> dst (cols x rows, ldd, sd)
+// through a 32 x 33 shared tile: reads along a src row and writes along a dst row are both
+// coalesced.
+__global__ void __launch_bounds__(256)
+    transpose_kernel(const float *__restrict__ src, long long lds, long long ss,
+                     float *__restrict__ dst, long long ldd, long long sd, int rows, int cols) {
+    __shared__ float tile[32][33];
+    const int b = blockIdx.z;
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    const float *sb = src + b * ss;
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        const int r = r0 + ty + j, c = c0 + tx;
+        tile[ty + j][tx] = (r < rows && c < cols) ? sb[static_cast<long long>(r) * lds + c] : 0.0f;
+    }
+    __syncthreads();
+    float *db = dst + b * sd;
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        const int c = c0 + ty + j, r = r0 + tx;  // dst row c, column r
+        if (c < cols && r < rows) db[static_cast<long long>(c) * ldd + r] = tile[tx][ty + j];
+    }
+}
+
+}  // namespace
+
+cudaError_t simt_untranspose(const SimtProblem &p, cudaStream_t stream, SimtProblem *q,
+                             const char **detail) {
+    *q = p;
+    q->transA = false;
+    q->transB = false;
+    if (!p.transA && !p.transB) return cudaSuccess;
+    // A broadcast operand (batch stride 0) is transposed once and stays broadcast.
+    const int nbA = (p.batch > 1 && p.strideA == 0) ? 1 : p.batch;
+    const int nbB = (p.batch > 1 && p.strideB == 0) ? 1 : p.batch;
+    const long long ldA = (static_cast<long long>(p.K) + 3) / 4 * 4;  // new A: M x K
+    const long long ldB = (static_cast<long long>(p.N) + 3) / 4 * 4;  // new B: K x N
+    const long long elemsA = p.transA ? static_cast<long long>(p.M) * ldA : 0;
+    const long long elemsB = p.transB ? static_cast<long long>(p.K) * ldB : 0;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) {
+        *detail = "cudaGetDevice failed";
+        return err;
+    }
+    float *ws = nullptr;
+    err = pack_workspace(dev, stream, kSlotTransposed,
+                         static_cast<size_t>(elemsA * nbA + elemsB * nbB) * 4, &ws);
+    if (err != cudaSuccess) {
+        *detail = "transpose workspace allocation failed";
+        return err;
+    }
+    if (p.transA) {  // A stored K x M -> M x K
+        dim3 grid((p.M + 31) / 32, (p.K + 31) / 32, nbA);
+        transpose_kernel<<<grid, 256, 0, stream>>>(p.A, p.lda, p.strideA, ws, ldA, elemsA, p.K,
+                                                   p.M);
+        q->A = ws;
+        q->lda = ldA;
+        q->strideA = nbA > 1 ? elemsA : 0;
+    }
+    if (p.transB) {  // B stored N x K -> K x N
+        float *wb = ws + elemsA * nbA;
+        dim3 grid((p.K + 31) / 32, (p.N + 31) / 32, nbB);
+        transpose_kernel<<<grid, 256, 0, stream>>>(p.B, p.ldb, p.strideB, wb, ldB, elemsB, p.N,
+                                                   p.K);
+        q->B = wb;
+        q->ldb = ldB;
+        q->strideB = nbB > 1 ? elemsB : 0;
+    }
+    err = cudaGetLastError();
+    if (err != cudaSuccess) *detail = "transpose kernel launch failed";
+    return err;
 }
 
 }  // namespace sg

@@ -40,6 +40,8 @@ struct SimtProblem {
     long long lda, ldb, ldc;
     long long strideA, strideB, strideC;  // element strides between batch entries
     int batch;
+    bool transA = false;  // A stored K x M (op(A) = A^T); the tile kernels take false only
+    bool transB = false;  // B stored N x K (op(B) = B^T); the tile kernels take false only
 };
 
 int simt_num_configs();
@@ -60,6 +62,12 @@ cudaError_t release_workspaces();
 
 // Frees the per-(device, stream) copies of operands repacked for TMA.
 cudaError_t release_pack_workspaces();
+
+// Turns a problem with transposed operands into the same product with row-major,
+// non-transposed, 16-byte aligned copies of those operands (written on `stream` into a
+// per-(device, stream) workspace). `q` receives the rewritten problem.
+cudaError_t simt_untranspose(const SimtProblem &p, cudaStream_t stream, SimtProblem *q,
+                             const char **detail);
 
 // Launches a one-thread kernel whose bounded wait can never be satisfied (which = 0: an
 // mbarrier, 1: a flag word), to exercise the timeout path.

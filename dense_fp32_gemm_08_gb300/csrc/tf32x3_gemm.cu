@@ -506,29 +506,54 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
     constexpr bool SMALL = PARTS == 2;
 
     {
-        const long long nrows = static_cast<long long>(p.M) * p.batch;
         const bool vecA = aligned16(p.A) && p.lda % 4 == 0 && (p.batch <= 1 || p.strideA % 4 == 0);
-        const dim3 rgrid(static_cast<unsigned>(std::min<long long>((p.K + 1023) / 1024, 8)),
-                         static_cast<unsigned>(std::min<long long>(nrows, 65535)));
-        if (vecA)
-            split_rows_kernel<true, SMALL><<<rgrid, 256, 0, stream>>>(
-                p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.M, p.K, p.batch);
-        else
-            split_rows_kernel<false, SMALL><<<rgrid, 256, 0, stream>>>(
-                p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.M, p.K, p.batch);
+        const bool vecB = aligned16(p.B) && p.ldb % 4 == 0 && (p.batch <= 1 || p.strideB % 4 == 0);
+        // A -> M x K (K contiguous): split in place, or split while transposing A stored K x M.
+        if (!p.transA) {
+            const long long nrows = static_cast<long long>(p.M) * p.batch;
+            const dim3 rgrid(static_cast<unsigned>(std::min<long long>((p.K + 1023) / 1024, 8)),
+                             static_cast<unsigned>(std::min<long long>(nrows, 65535)));
+            if (vecA)
+                split_rows_kernel<true, SMALL><<<rgrid, 256, 0, stream>>>(
+                    p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.M, p.K, p.batch);
+            else
+                split_rows_kernel<false, SMALL><<<rgrid, 256, 0, stream>>>(
+                    p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.M, p.K, p.batch);
+        } else {
+            dim3 grid((p.M + 31) / 32, (p.K + 31) / 32, p.batch);
+            if (vecA)
+                split_transpose_kernel<true, SMALL><<<grid, 256, 0, stream>>>(
+                    p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.K, p.M);
+            else
+                split_transpose_kernel<false, SMALL><<<grid, 256, 0, stream>>>(
+                    p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.K, p.M);
+        }
         err = cudaGetLastError();
         if (err != cudaSuccess) {
             *detail = "split kernel launch failed";
             return err;
         }
-        const bool vecB = aligned16(p.B) && p.ldb % 4 == 0 && (p.batch <= 1 || p.strideB % 4 == 0);
-        dim3 grid((p.N + 31) / 32, (p.K + 31) / 32, p.batch);
-        if (vecB)
-            split_transpose_kernel<true, SMALL><<<grid, 256, 0, stream>>>(
-                p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.K, p.N);
-        else
-            split_transpose_kernel<false, SMALL><<<grid, 256, 0, stream>>>(
-                p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.K, p.N);
+        // B -> N x K (K contiguous): split while transposing B stored K x N, or in place when
+        // B is stored transposed (N x K).
+        if (!p.transB) {
+            dim3 grid((p.N + 31) / 32, (p.K + 31) / 32, p.batch);
+            if (vecB)
+                split_transpose_kernel<true, SMALL><<<grid, 256, 0, stream>>>(
+                    p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.K, p.N);
+            else
+                split_transpose_kernel<false, SMALL><<<grid, 256, 0, stream>>>(
+                    p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.K, p.N);
+        } else {
+            const long long nrows = static_cast<long long>(p.N) * p.batch;
+            const dim3 rgrid(static_cast<unsigned>(std::min<long long>((p.K + 1023) / 1024, 8)),
+                             static_cast<unsigned>(std::min<long long>(nrows, 65535)));
+            if (vecB)
+                split_rows_kernel<true, SMALL><<<rgrid, 256, 0, stream>>>(
+                    p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.N, p.K, p.batch);
+            else
+                split_rows_kernel<false, SMALL><<<rgrid, 256, 0, stream>>>(
+                    p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.N, p.K, p.batch);
+        }
         err = cudaGetLastError();
         if (err != cudaSuccess) {
             *detail = "split-transpose kernel launch failed";

@@ -57,6 +57,19 @@ typedef enum sgemm_status {
     SGEMM_ERR_UNSUPPORTED = 4    /* valid arguments this build cannot run (e.g. no GPU) */
 } sgemm_status_t;
 
+/* Operand form (BLAS transa / transb, row-major storage). */
+typedef enum sgemm_op {
+    SGEMM_OP_N = 0, /* the operand as stored: A is M x K (lda >= K), B is K x N (ldb >= N) */
+    SGEMM_OP_T = 1  /* its transpose: A stored K x M (lda >= M), B stored N x K (ldb >= K) */
+} sgemm_op_t;
+
+/* Arithmetic path (the accuracy / speed knob of sgemm_ex). */
+typedef enum sgemm_path {
+    SGEMM_PATH_SIMT = 0,   /* fp32 FMAs on the SIMT cores: the sgemm() path */
+    SGEMM_PATH_3XTF32 = 1, /* three TF32 tensor-core products: the sgemm_3xtf32() path */
+    SGEMM_PATH_TF32 = 2    /* one TF32 tensor-core product: the sgemm_tf32() path */
+} sgemm_path_t;
+
 /*
  * C = alpha * (A . B) + beta * C on the FP32 SIMT path ("GEMM scrapbook": 2D block tiling
  * with register outer products, float4 loads, warp tiling and double buffering; here a
@@ -154,6 +167,31 @@ sgemm_status_t sgemm_tf32_strided_batched(int64_t M, int64_t N, int64_t K, float
 sgemm_status_t sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                              const float *A, int64_t lda, const float *B, int64_t ldb,
                              float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * C = alpha * (op(A) . op(B)) + beta * C with op(X) = X or X^T, on the chosen path. The pages
+ * multiply row-major A by row-major B only ("a CUDA matmul", section 02); the transposed
+ * forms are the BLAS generalisation. op(A) is M x K and op(B) is K x N; a transposed operand
+ * is stored with its rows and columns swapped (A: K x M with lda >= max(1, M); B: N x K with
+ * ldb >= max(1, K)). Column-major callers can use the identity C^T = B^T A^T: a column-major
+ * M x N product is the row-major N x M product with A and B exchanged.
+ * On the SIMT path each transposed operand is first transposed once into a per-(device,
+ * stream) workspace; the TF32 paths transpose inside their split pre-pass. Arguments,
+ * errors and conventions are otherwise those of sgemm() / sgemm_strided_batched(); an
+ * unknown `transa`, `transb` or `path` returns SGEMM_ERR_INVALID_VALUE.
+ */
+sgemm_status_t sgemm_ex(sgemm_op_t transa, sgemm_op_t transb, sgemm_path_t path,
+                        int64_t M, int64_t N, int64_t K, float alpha,
+                        const float *A, int64_t lda, const float *B, int64_t ldb,
+                        float beta, float *C, int64_t ldc, void *stream);
+
+/* Batched form of sgemm_ex (strides as in sgemm_strided_batched, of the stored operands). */
+sgemm_status_t sgemm_ex_strided_batched(sgemm_op_t transa, sgemm_op_t transb, sgemm_path_t path,
+                                        int64_t M, int64_t N, int64_t K, float alpha,
+                                        const float *A, int64_t lda, int64_t strideA,
+                                        const float *B, int64_t ldb, int64_t strideB,
+                                        float beta, float *C, int64_t ldc, int64_t strideC,
+                                        int64_t batch, void *stream);
 
 /* Static text for a status code (never NULL). */
 const char *sgemm_status_string(sgemm_status_t status);

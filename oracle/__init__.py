@@ -60,6 +60,13 @@ def _bind(lib):
     lib.sgemm_ref_rows.restype = ctypes.c_int
     lib.sgemm_ref_absdot_rows.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, p, i64]
     lib.sgemm_ref_absdot_rows.restype = ctypes.c_int
+    i32 = ctypes.c_int
+    lib.sgemm_ref_ex_rows.argtypes = [i32, i32, i64, i64, i64, f64, p, i64, p, i64, f64, p, i64,
+                                      p, i64, p, i64]
+    lib.sgemm_ref_ex_rows.restype = ctypes.c_int
+    lib.sgemm_ref_absdot_ex_rows.argtypes = [i32, i32, i64, i64, i64, p, i64, p, i64, p, i64,
+                                             p, i64]
+    lib.sgemm_ref_absdot_ex_rows.restype = ctypes.c_int
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
     return lib
@@ -99,6 +106,43 @@ def sgemm(M: int, N: int, K: int, alpha: float, A: np.ndarray, lda: int, B: np.n
     if st != 0:
         raise ValueError(f"oracle rejected the arguments (status {st})")
     return out
+
+
+def sgemm_ex(transa: bool, transb: bool, M: int, N: int, K: int, alpha: float, A: np.ndarray,
+             lda: int, B: np.ndarray, ldb: int, beta: float, C: np.ndarray | None, ldc: int,
+             rows=None, lib=None) -> np.ndarray:
+    """Like ``sgemm`` with transposed operands: A stored K x M when ``transa``, B stored
+    N x K when ``transb`` (row-major, BLAS convention)."""
+    lib = lib or load()
+    A = _as_f32(A)
+    B = _as_f32(B)
+    C = None if C is None else _as_f32(C)
+    idx = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    R = M if idx is None else len(idx)
+    out = np.empty((R, N), dtype=np.float32)
+    st = lib.sgemm_ref_ex_rows(int(bool(transa)), int(bool(transb)), M, N, K, float(alpha),
+                               _ptr(A), lda, _ptr(B), ldb, float(beta), _ptr(C), ldc, _ptr(idx),
+                               0 if idx is None else len(idx), _ptr(out), max(N, 1))
+    if st != 0:
+        raise ValueError(f"oracle rejected the arguments (status {st})")
+    return out
+
+
+def absdot_ex(transa: bool, transb: bool, M: int, N: int, K: int, A: np.ndarray, lda: int,
+              B: np.ndarray, ldb: int, rows=None, lib=None) -> np.ndarray:
+    """fp64 sum_k |op(A)[i][k]| * |op(B)[k][j]| for the listed rows."""
+    lib = lib or load()
+    A = _as_f32(A)
+    B = _as_f32(B)
+    idx = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    R = M if idx is None else len(idx)
+    den = np.empty((R, N), dtype=np.float64)
+    st = lib.sgemm_ref_absdot_ex_rows(int(bool(transa)), int(bool(transb)), M, N, K, _ptr(A),
+                                      lda, _ptr(B), ldb, _ptr(idx),
+                                      0 if idx is None else len(idx), _ptr(den), max(N, 1))
+    if st != 0:
+        raise ValueError(f"oracle rejected the arguments (status {st})")
+    return den
 
 
 def absdot(M: int, N: int, K: int, A: np.ndarray, lda: int, B: np.ndarray, ldb: int,

@@ -122,6 +122,87 @@ int sgemm_ref_absdot_rows(int64_t M, int64_t N, int64_t K,
     return ORACLE_OK;
 }
 
+/*
+ * The same product with transposed operands (BLAS transa / transb, row-major storage):
+ *   op(A)[i][k] = transa ? A[k * lda + i] : A[i * lda + k]   (A stored K x M when transposed)
+ *   op(B)[k][j] = transb ? B[j * ldb + k] : B[k * ldb + j]   (B stored N x K when transposed)
+ *   out[i][j]   = fl32( alpha * sum_k op(A)[i][k] * op(B)[k][j] + beta * C[i][j] )
+ * with the same readings as sgemm_ref_rows (fp64 sum in ascending k, beta == 0 leaves C unread,
+ * alpha == 0 leaves A and B unread). Leading dimensions: lda >= max(1, transa ? M : K),
+ * ldb >= max(1, transb ? K : N), ldc, ldo >= max(1, N).
+ */
+int sgemm_ref_ex_rows(int transa, int transb, int64_t M, int64_t N, int64_t K, double alpha,
+                      const float *A, int64_t lda, const float *B, int64_t ldb,
+                      double beta, const float *C, int64_t ldc,
+                      const int64_t *rows, int64_t nrows, float *out, int64_t ldo) {
+    if (M < 0 || N < 0 || K < 0) return ORACLE_BAD_ARGS;
+    const int64_t a_cols = transa ? M : K, b_cols = transb ? K : N;
+    if (lda < (a_cols > 1 ? a_cols : 1) || ldb < (b_cols > 1 ? b_cols : 1)) return ORACLE_BAD_ARGS;
+    if (ldc < (N > 1 ? N : 1) || ldo < (N > 1 ? N : 1)) return ORACLE_BAD_ARGS;
+    const int64_t R = rows ? nrows : M;
+    if (R < 0) return ORACLE_BAD_ARGS;
+    for (int64_t r = 0; rows && r < R; ++r)
+        if (rows[r] < 0 || rows[r] >= M) return ORACLE_BAD_ARGS;
+    if (R == 0 || N == 0) return ORACLE_OK;
+    int failed = 0;
+
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)N * sizeof(double));
+        if (!acc) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < R; ++r) {
+            if (!acc) continue;
+            const int64_t i = rows ? rows[r] : r;
+            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;
+            if (alpha != 0.0) {
+                for (int64_t k = 0; k < K; ++k) {
+                    const double a = (double)(transa ? A[k * lda + i] : A[i * lda + k]);
+                    for (int64_t j = 0; j < N; ++j)
+                        acc[j] += a * (double)(transb ? B[j * ldb + k] : B[k * ldb + j]);
+                }
+            }
+            float *orow = out + r * ldo;
+            for (int64_t j = 0; j < N; ++j) {
+                double v = (alpha != 0.0) ? alpha * acc[j] : 0.0;
+                if (beta != 0.0) v += beta * (double)C[i * ldc + j];
+                orow[j] = (float)v;
+            }
+        }
+        free(acc);
+    }
+    return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+/* sum_k |op(A)[i][k]| * |op(B)[k][j]| in fp64 for the listed rows (transposes as above). */
+int sgemm_ref_absdot_ex_rows(int transa, int transb, int64_t M, int64_t N, int64_t K,
+                             const float *A, int64_t lda, const float *B, int64_t ldb,
+                             const int64_t *rows, int64_t nrows, double *den, int64_t ldd) {
+    if (M < 0 || N < 0 || K < 0) return ORACLE_BAD_ARGS;
+    const int64_t a_cols = transa ? M : K, b_cols = transb ? K : N;
+    if (lda < (a_cols > 1 ? a_cols : 1) || ldb < (b_cols > 1 ? b_cols : 1)) return ORACLE_BAD_ARGS;
+    if (ldd < (N > 1 ? N : 1)) return ORACLE_BAD_ARGS;
+    const int64_t R = rows ? nrows : M;
+    if (R < 0) return ORACLE_BAD_ARGS;
+    for (int64_t r = 0; rows && r < R; ++r)
+        if (rows[r] < 0 || rows[r] >= M) return ORACLE_BAD_ARGS;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < R; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        double *drow = den + r * ldd;
+        for (int64_t j = 0; j < N; ++j) drow[j] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double a = fabs((double)(transa ? A[k * lda + i] : A[i * lda + k]));
+            for (int64_t j = 0; j < N; ++j)
+                drow[j] += a * fabs((double)(transb ? B[j * ldb + k] : B[k * ldb + j]));
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* Threads the two loops above use (OpenMP over result rows). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -15,6 +15,8 @@ Sources of each pin:
   for beta = 0 (C not read), alpha = 0 (A, B not read) and K = 0.
 * cancellation: terms exactly representable in fp32 whose running sum needs more than 24
   bits; the exact sum is representable, so one final rounding reproduces it.
+* transposes: stored transposes through the ex entry agree with the plain product on
+  numpy-transposed copies, with exact rational brute force, and with identity products.
 * brute force: exact rational arithmetic (fractions.Fraction) on tiny shapes, rounded once
   to fp32; the oracle may differ by at most one fp32 ulp (its fp64 sum rounds before the
   final rounding).
@@ -191,6 +193,60 @@ def pin_row_subset(lib):
     return np.array_equal(sub, full[rows])
 
 
+def _ex(lib, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, rows=None):
+    return oracle.sgemm_ex(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, rows=rows, lib=lib)
+
+
+def pin_transposed_identity(lib):
+    # I^T = I: op(A) = (A^T stored) with B = I gives back A, for every transpose flag.
+    M, K = 9, 13
+    A = synth.uniform(M, K, 61)
+    At = np.ascontiguousarray(A.T)                # K x M storage of A^T
+    eye = np.eye(K, dtype=np.float32)
+    for tb in (False, True):
+        if not np.array_equal(_ex(lib, True, tb, M, K, K, 1.0, At, M, eye, K, 0.0, None, K), A):
+            return False
+        if not np.array_equal(_ex(lib, False, tb, M, K, K, 1.0, A, K, eye, K, 0.0, None, K), A):
+            return False
+    return True
+
+
+def pin_transposed_against_plain(lib):
+    # op(A) op(B) on stored transposes equals the plain product on numpy-transposed copies
+    # (numpy's transpose is a separate routine); padded leading dimensions included.
+    M, N, K = 11, 7, 19
+    A = synth.normal(M, K, 71)
+    B = synth.normal(K, N, 72)
+    C = synth.normal(M, N, 73)
+    plain = _mm(lib, M, N, K, 0.7, A, K, B, N, -1.3, C, N)
+    At = synth.padded(np.ascontiguousarray(A.T), M + 2)   # K x (M + 2)
+    Bt = synth.padded(np.ascontiguousarray(B.T), K + 3)   # N x (K + 3)
+    for ta, tb, a, lda, b, ldb in [(False, False, A, K, B, N), (True, False, At, M + 2, B, N),
+                                   (False, True, A, K, Bt, K + 3), (True, True, At, M + 2, Bt, K + 3)]:
+        got = _ex(lib, ta, tb, M, N, K, 0.7, a, lda, b, ldb, -1.3, C, N)
+        if not np.array_equal(got, plain):
+            return False
+    return True
+
+
+def pin_transposed_brute_force(lib):
+    for n, (M, N, K) in enumerate([(1, 1, 1), (2, 3, 4), (5, 2, 3), (3, 7, 6)]):
+        A = synth.normal(M, K, 400 + n)
+        B = synth.normal(K, N, 500 + n)
+        C = synth.normal(M, N, 600 + n)
+        At, Bt = np.ascontiguousarray(A.T), np.ascontiguousarray(B.T)
+        for ta in (False, True):
+            for tb in (False, True):
+                out = _ex(lib, ta, tb, M, N, K, 0.7, At if ta else A, M if ta else K,
+                          Bt if tb else B, K if tb else N, -1.3, C, N)
+                for i in range(M):
+                    for j in range(N):
+                        exact = float(_exact_cell(A, B, C, i, j, 0.7, -1.3))
+                        if abs(float(out[i, j]) - exact) > _ulp32(exact):
+                            return False
+    return True
+
+
 PINS = {
     "identity": pin_identity,
     "permutation": pin_permutation,
@@ -201,4 +257,7 @@ PINS = {
     "cancellation": pin_cancellation,
     "leading_dims": pin_leading_dims,
     "row_subset": pin_row_subset,
+    "transposed_identity": pin_transposed_identity,
+    "transposed_against_plain": pin_transposed_against_plain,
+    "transposed_brute_force": pin_transposed_brute_force,
 }

@@ -77,6 +77,21 @@ def test_invalid_arguments(sgemm_lib, args, why):
         assert why in L.sgemm_last_error().decode()
 
 
+def test_ex_argument_rules(sgemm_lib):
+    L = sgemm_lib.lib()
+    # transposed A: lda >= M; transposed B: ldb >= K
+    ok_t = (1, 1, 0, 8, 6, 4, 1.0, FAKE, 8, FAKE, 4, 0.0, FAKE, 6, None)
+    assert L.sgemm_ex(*ok_t) != sgemm_lib.SGEMM_ERR_INVALID_VALUE
+    bad_lda = (1, 0, 0, 8, 6, 4, 1.0, FAKE, 7, FAKE, 6, 0.0, FAKE, 6, None)
+    assert L.sgemm_ex(*bad_lda) == sgemm_lib.SGEMM_ERR_INVALID_VALUE
+    assert "transposed" in L.sgemm_last_error().decode()
+    bad_ldb = (0, 1, 0, 8, 6, 4, 1.0, FAKE, 4, FAKE, 3, 0.0, FAKE, 6, None)
+    assert L.sgemm_ex(*bad_ldb) == sgemm_lib.SGEMM_ERR_INVALID_VALUE
+    for bad in ((2, 0, 0), (0, 5, 0), (0, 0, 9)):
+        args = bad + (8, 6, 4, 1.0, FAKE, 8, FAKE, 6, 0.0, FAKE, 6, None)
+        assert L.sgemm_ex(*args) == sgemm_lib.SGEMM_ERR_INVALID_VALUE
+
+
 def test_invalid_batched_arguments(sgemm_lib):
     L = sgemm_lib.lib()
     base = [8, 8, 8, 1.0, FAKE, 8, 64, FAKE, 8, 64, 0.0, FAKE, 8, 64, 2, None]

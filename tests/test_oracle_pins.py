@@ -40,6 +40,10 @@ MUTANTS = {
                        "if (beta != 0.0) v += alpha * beta * (double)C[i * ldc + j];"),
     "ld_ignored": ("const float *brow = B + k * ldb;\n                    for (int64_t j = 0; j < N; ++j) acc[j] += a",
                    "const float *brow = B + k * N;\n                    for (int64_t j = 0; j < N; ++j) acc[j] += a"),
+    "ex_transposed_A_index": ("const double a = (double)(transa ? A[k * lda + i] : A[i * lda + k]);",
+                              "const double a = (double)(transa ? A[i * lda + k] : A[i * lda + k]);"),
+    "ex_transposed_B_index": ("acc[j] += a * (double)(transb ? B[j * ldb + k] : B[k * ldb + j]);",
+                              "acc[j] += a * (double)(transb ? B[k * ldb + j] : B[k * ldb + j]);"),
     "wrong_row_index": ("const int64_t i = rows ? rows[r] : r;\n            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;",
                         "const int64_t i = r;\n            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;"),
 }
