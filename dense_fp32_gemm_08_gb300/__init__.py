@@ -17,7 +17,7 @@ from pathlib import Path
 __all__ = [
     "SgemmError", "library_path", "lib", "sgemm", "sgemm_strided_batched", "sgemm_3xtf32",
     "sgemm_3xtf32_strided_batched", "sgemm_tf32", "sgemm_tf32_strided_batched", "sgemm_ex",
-    "sgemm_ex_strided_batched", "sgemm_noalloc", "sgemm_status_string", "sgemm_last_error",
+    "sgemm_ex_strided_batched", "sgemm_fused", "sgemm_fused_strided_batched", "sgemm_noalloc", "sgemm_status_string", "sgemm_last_error",
     "sgemm_device_status", "sgemm_release_workspace", "sgemm_num_configs",
     "sgemm_config_name", "sgemm_select_config", "sgemm_force_config",
     "sgemm_selftest_bounded_wait", "matmul",
@@ -34,6 +34,7 @@ SGEMM_ERR_UNSUPPORTED = 4
 SGEMM_OP_N, SGEMM_OP_T = 0, 1
 SGEMM_PATH_SIMT, SGEMM_PATH_3XTF32, SGEMM_PATH_TF32 = 0, 1, 2
 _PATHS = {"simt": SGEMM_PATH_SIMT, "3xtf32": SGEMM_PATH_3XTF32, "tf32": SGEMM_PATH_TF32}
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2, "gelu_tanh": 3, "silu": 4}
 
 _LIBRARY = Path(__file__).resolve().with_name("libsgemm_gb300.so")
 _lib = None
@@ -75,6 +76,10 @@ def _bind(L):
     L.sgemm_ex.restype = i32
     L.sgemm_ex_strided_batched.argtypes = [i32, i32, i32] + batched
     L.sgemm_ex_strided_batched.restype = i32
+    L.sgemm_fused.argtypes = [i32, i32, i32] + gemm[:-1] + [p, i32, p]
+    L.sgemm_fused.restype = i32
+    L.sgemm_fused_strided_batched.argtypes = [i32, i32, i32] + batched[:-1] + [p, i32, p]
+    L.sgemm_fused_strided_batched.restype = i32
     L.sgemm_status_string.argtypes = [i32]
     L.sgemm_status_string.restype = ctypes.c_char_p
     L.sgemm_last_error.argtypes = []
@@ -195,6 +200,27 @@ def sgemm_ex_strided_batched(transa, transb, M, N, K, alpha, A, lda, strideA, B,
     _check(lib().sgemm_ex_strided_batched(_op(transa), _op(transb), pth, M, N, K, alpha, _ptr(A),
                                           lda, strideA, _ptr(B), ldb, strideB, beta, _ptr(C), ldc,
                                           strideC, batch, _stream(stream)))
+
+
+def sgemm_fused(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias=None,
+                act="none", path="simt", stream=None) -> None:
+    """C = act(alpha * op(A) op(B) + bias) + beta * C; act is 'none', 'relu', 'gelu',
+    'gelu_tanh' or 'silu' (or its enum value); bias is an N-vector or None."""
+    pth = _PATHS.get(path, path) if isinstance(path, str) else int(path)
+    code = ACTIVATIONS[act] if isinstance(act, str) else int(act)
+    _check(lib().sgemm_fused(_op(transa), _op(transb), pth, M, N, K, alpha, _ptr(A), lda,
+                             _ptr(B), ldb, beta, _ptr(C), ldc, _ptr(bias), code, _stream(stream)))
+
+
+def sgemm_fused_strided_batched(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
+                                beta, C, ldc, strideC, batch, bias=None, act="none", path="simt",
+                                stream=None) -> None:
+    pth = _PATHS.get(path, path) if isinstance(path, str) else int(path)
+    code = ACTIVATIONS[act] if isinstance(act, str) else int(act)
+    _check(lib().sgemm_fused_strided_batched(_op(transa), _op(transb), pth, M, N, K, alpha,
+                                             _ptr(A), lda, strideA, _ptr(B), ldb, strideB, beta,
+                                             _ptr(C), ldc, strideC, batch, _ptr(bias), code,
+                                             _stream(stream)))
 
 
 def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:

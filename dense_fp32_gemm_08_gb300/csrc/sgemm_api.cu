@@ -8,6 +8,7 @@
 #include <cstring>
 
 #include "config_table.h"
+#include "epilogue.cuh"
 #include "ptx.cuh"
 #include "simt_gemm.cuh"
 #include "tf32x3_gemm.cuh"
@@ -55,17 +56,25 @@ bool log_enabled() {
     return on;
 }
 
-// C = beta * C (zeros when beta == 0, C not read then). Rows over the grid's y dimension
+// C = beta * C (zeros when beta == 0, C not read then), the whole product when alpha == 0 or
+// K == 0; with a fused epilogue, C = act(bias) + beta * C. Rows over the grid's y dimension
 // (batch entries stacked), columns over threads.
 __global__ void scale_c_kernel(float *C, long long M, long long N, long long ldc,
-                               long long strideC, long long batch, float beta) {
+                               long long strideC, long long batch, float beta,
+                               const float *bias, int act) {
     const long long nrows = M * batch;
+    const bool fused = bias != nullptr || act != sg::kActNone;
     for (long long gr = blockIdx.y; gr < nrows; gr += gridDim.y) {
         const long long b = gr / M, r = gr - b * M;
         float *row = C + b * strideC + r * ldc;
         for (long long c = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; c < N;
-             c += static_cast<long long>(gridDim.x) * blockDim.x)
-            row[c] = beta == 0.0f ? 0.0f : beta * row[c];
+             c += static_cast<long long>(gridDim.x) * blockDim.x) {
+            if (fused)
+                row[c] = sg::epilogue_value(0.0f, 0.0f, beta, bias, static_cast<int>(c), act,
+                                            row + c);
+            else
+                row[c] = beta == 0.0f ? 0.0f : beta * row[c];
+        }
     }
 }
 
@@ -80,6 +89,8 @@ struct Args {
     long long ldc, sC;
     long long batch;
     bool ta = false, tb = false;  // A stored K x M, B stored N x K
+    const float *bias = nullptr;  // fused epilogue
+    int act = 0;
 };
 
 // Checks shared by every entry point. Returns SGEMM_OK when the arguments are valid.
@@ -115,7 +126,8 @@ sgemm_status_t run_scale(const Args &a, cudaStream_t stream) {
     const long long nrows = a.M * a.batch;
     const dim3 grid(static_cast<unsigned>((a.N + 255) / 256 < 8 ? (a.N + 255) / 256 : 8),
                     static_cast<unsigned>(nrows < 65535 ? nrows : 65535));
-    scale_c_kernel<<<grid, 256, 0, stream>>>(a.C, a.M, a.N, a.ldc, a.sC, a.batch, a.beta);
+    scale_c_kernel<<<grid, 256, 0, stream>>>(a.C, a.M, a.N, a.ldc, a.sC, a.batch, a.beta, a.bias,
+                                             a.act);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return fail_cuda("scale kernel launch", err);
     return SGEMM_OK;
@@ -140,6 +152,8 @@ sg::SimtProblem to_problem(const Args &a) {
     p.batch = static_cast<int>(a.batch);
     p.transA = a.ta;
     p.transB = a.tb;
+    p.bias = a.bias;
+    p.act = a.act;
     return p;
 }
 
@@ -278,6 +292,42 @@ sgemm_status_t sgemm_selftest_bounded_wait(int which, void *stream_ptr) {
     cudaError_t err = sg::simt_selftest_wait(which, static_cast<cudaStream_t>(stream_ptr));
     if (err != cudaSuccess) return fail_cuda("self-test kernel launch", err);
     return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_fused_strided_batched(sgemm_op_t transa, sgemm_op_t transb,
+                                           sgemm_path_t path, int64_t M, int64_t N, int64_t K,
+                                           float alpha, const float *A, int64_t lda,
+                                           int64_t strideA, const float *B, int64_t ldb,
+                                           int64_t strideB, float beta, float *C, int64_t ldc,
+                                           int64_t strideC, int64_t batch, const float *bias,
+                                           sgemm_activation_t act, void *stream) {
+    t_last_error[0] = '\0';
+    if (act < SGEMM_ACT_NONE || act > SGEMM_ACT_SILU)
+        return fail(SGEMM_ERR_INVALID_VALUE, "unknown activation");
+    if ((transa != SGEMM_OP_N && transa != SGEMM_OP_T) ||
+        (transb != SGEMM_OP_N && transb != SGEMM_OP_T))
+        return fail(SGEMM_ERR_INVALID_VALUE, "transa and transb must be SGEMM_OP_N or SGEMM_OP_T");
+    Path pth;
+    switch (path) {
+        case SGEMM_PATH_SIMT: pth = kPathSimt; break;
+        case SGEMM_PATH_3XTF32: pth = kPathTf32x3; break;
+        case SGEMM_PATH_TF32: pth = kPathTf32; break;
+        default: return fail(SGEMM_ERR_INVALID_VALUE, "unknown path");
+    }
+    Args a{M, N, K, alpha, beta, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch};
+    a.ta = transa == SGEMM_OP_T;
+    a.tb = transb == SGEMM_OP_T;
+    a.bias = bias;
+    a.act = static_cast<int>(act);
+    return dispatch(a, stream, pth);
+}
+
+sgemm_status_t sgemm_fused(sgemm_op_t transa, sgemm_op_t transb, sgemm_path_t path, int64_t M,
+                           int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                           const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                           const float *bias, sgemm_activation_t act, void *stream) {
+    return sgemm_fused_strided_batched(transa, transb, path, M, N, K, alpha, A, lda, 0, B, ldb, 0,
+                                       beta, C, ldc, 0, 1, bias, act, stream);
 }
 
 sgemm_status_t sgemm_ex_strided_batched(sgemm_op_t transa, sgemm_op_t transb, sgemm_path_t path,

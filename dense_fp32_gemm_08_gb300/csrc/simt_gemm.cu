@@ -24,6 +24,7 @@
 //      ("float4" chapter: 128-bit loads), no transposed copy of A is needed.
 //  * Epilogue: alpha * acc + beta * C fused, float4 loads and stores where C allows,
 //    C never read when beta == 0.
+#include "epilogue.cuh"
 #include "ptx.cuh"
 #include "simt_gemm.cuh"
 #include "skinny_gemm.cuh"
@@ -51,6 +52,8 @@ struct KParams {
     int batch;
     int tiles_m, tiles_n, group_m;
     int a_vec4, b_vec4, c_vec4;
+    const float *bias;  // fused epilogue (nullptr: none)
+    int act;            // fused epilogue activation (0: none)
 };
 
 // Grouped raster order: GROUP_M consecutive tile rows are swept column by column, so CTAs
@@ -162,10 +165,12 @@ __device__ __forceinline__ void cp_async_stage(float *sA, float *sB, const KPara
     }
 }
 
-// alpha * acc + beta * C for the thread's 8 x 16 cells (rows tr + 8r, cols 16q + 4tc + e).
+// alpha * acc + beta * C for the thread's 8 x 16 cells (rows tr + 8r, cols 16q + 4tc + e);
+// with a bias or an activation, the fused form act(alpha * acc + bias) + beta * C.
 __device__ __forceinline__ void epilogue(const KParams &p, float *Cb, int row0, int col0,
                                          const float2 (&acc)[8][8]) {
     const float alpha = p.alpha, beta = p.beta;
+    const bool fused = p.bias != nullptr || p.act != kActNone;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         const int gm = row0 + 8 * r;
@@ -176,7 +181,13 @@ __device__ __forceinline__ void epilogue(const KParams &p, float *Cb, int row0, 
             const int gn = col0 + 16 * q;
             const float v[4] = {acc[r][2 * q].x, acc[r][2 * q].y, acc[r][2 * q + 1].x,
                                 acc[r][2 * q + 1].y};
-            if (p.c_vec4 && gn + 3 < p.N) {
+            if (fused) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (gn + e < p.N)
+                        crow[gn + e] = epilogue_value(v[e], alpha, beta, p.bias, gn + e, p.act,
+                                                      crow + gn + e);
+            } else if (p.c_vec4 && gn + 3 < p.N) {
                 float4 o;
                 if (beta != 0.0f) {
                     const float4 c = *reinterpret_cast<const float4 *>(crow + gn);
@@ -731,6 +742,8 @@ cudaError_t launch_impl(int id, const SimtProblem &p, cudaStream_t stream, const
     kp.a_vec4 = operand_vec4(p.A, p.lda, p.strideA, p.batch);
     kp.b_vec4 = operand_vec4(p.B, p.ldb, p.strideB, p.batch);
     kp.c_vec4 = operand_vec4(p.C, p.ldc, p.strideC, p.batch);
+    kp.bias = p.bias;
+    kp.act = p.act;
 
     CUtensorMap mapA, mapB;
     memset(&mapA, 0, sizeof(mapA));
@@ -883,6 +896,8 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
     kp.a_vec4 = operand_vec4(p.A, p.lda, p.strideA, p.batch);
     kp.b_vec4 = operand_vec4(p.B, p.ldb, p.strideB, p.batch);
     kp.c_vec4 = operand_vec4(p.C, p.ldc, p.strideC, p.batch);
+    kp.bias = p.bias;
+    kp.act = p.act;
 
     const long long tiles_per_batch = static_cast<long long>(kp.tiles_m) * kp.tiles_n;
     const long long T = tiles_per_batch * p.batch;
@@ -1122,6 +1137,8 @@ cudaError_t simt_launch_noalloc(const SimtProblem &p, cudaStream_t stream, const
     kp.a_vec4 = 1;
     kp.b_vec4 = 1;
     kp.c_vec4 = operand_vec4(p.C, p.ldc, p.strideC, p.batch);
+    kp.bias = nullptr;  // plain product only
+    kp.act = 0;
 
     const long long tiles_per_batch = static_cast<long long>(kp.tiles_m) * kp.tiles_n;
     const long long T = tiles_per_batch * p.batch;

@@ -42,6 +42,8 @@ struct SimtProblem {
     int batch;
     bool transA = false;  // A stored K x M (op(A) = A^T); the tile kernels take false only
     bool transB = false;  // B stored N x K (op(B) = B^T); the tile kernels take false only
+    const float *bias = nullptr;  // fused epilogue: per-column bias (N values), or none
+    int act = 0;                  // fused epilogue: Activation (epilogue.cuh)
 };
 
 int simt_num_configs();

@@ -15,6 +15,7 @@
 //   workspace is used, and results are deterministic.
 #include <cooperative_groups.h>
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 #include "skinny_gemm.cuh"
 
@@ -76,7 +77,7 @@ __global__ void __launch_bounds__(256) skinny_tall_kernel(SkinnyProblem p) {
             for (int n = 1; n < NN; ++n)
                 if (lane == n) s = acc[n];
             float *c = p.C + b * p.strideC + row * p.ldc + lane;
-            *c = p.beta != 0.0f ? fmaf(p.alpha, s, p.beta * *c) : p.alpha * s;
+            *c = epilogue_value(s, p.alpha, p.beta, p.bias, lane, p.act, c);
         }
     }
 }
@@ -167,7 +168,7 @@ __global__ void __cluster_dims__(1, kCluster, 1) __launch_bounds__(kWideWarps * 
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (n0 + e < p.N)
-                    c[e] = p.beta != 0.0f ? fmaf(p.alpha, sv[e], p.beta * c[e]) : p.alpha * sv[e];
+                    c[e] = epilogue_value(sv[e], p.alpha, p.beta, p.bias, n0 + e, p.act, c + e);
         }
     }
     cluster.sync();  // no CTA leaves while CTA 0 may still read its shared memory

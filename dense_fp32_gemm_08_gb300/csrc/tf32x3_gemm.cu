@@ -31,6 +31,7 @@
 // parts (tf32_rna of each value) and the kernel issues big_A.big_B alone, with twice the
 // stages in the same shared memory. Each product is then off by at most (2u + u^2)|a b|,
 // u = 2^-11, so the result carries TF32 rather than fp32 accuracy.
+#include "epilogue.cuh"
 #include "ptx.cuh"
 #include "tf32x3_gemm.cuh"
 
@@ -223,6 +224,8 @@ struct TParams {
     int batch;
     int tiles_m, tiles_n;
     int c_vec4;
+    const float *bias;  // fused epilogue (nullptr: none)
+    int act;            // fused epilogue activation (0: none)
 };
 
 template <int BN, int STAGES, int ACCS, int PRODUCTS>
@@ -347,7 +350,15 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 if (row >= p.M) continue;
                 const int col0 = n0 + c0;
-                if (p.c_vec4 && col0 + 31 < p.N) {
+                if (p.bias != nullptr || p.act != kActNone) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = col0 + j;
+                        if (col < p.N)
+                            crow[col] = epilogue_value(v[j], alpha, beta, p.bias, col, p.act,
+                                                       crow + col);
+                    }
+                } else if (p.c_vec4 && col0 + 31 < p.N) {
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
                         float4 o;
@@ -582,6 +593,8 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
     tp.tiles_m = (p.M + BM - 1) / BM;
     tp.tiles_n = (p.N + BN - 1) / BN;
     tp.c_vec4 = aligned16(p.C) && p.ldc % 4 == 0 && (p.batch <= 1 || p.strideC % 4 == 0);
+    tp.bias = p.bias;
+    tp.act = p.act;
     const long long tiles = static_cast<long long>(tp.tiles_m) * tp.tiles_n;
     if (tiles > 0x7fffffffLL || p.batch > 65535) {
         *detail = "too many output tiles or batch entries for the 3xTF32 grid";

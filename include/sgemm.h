@@ -70,6 +70,15 @@ typedef enum sgemm_path {
     SGEMM_PATH_TF32 = 2    /* one TF32 tensor-core product: the sgemm_tf32() path */
 } sgemm_path_t;
 
+/* Activation of the fused epilogue (sgemm_fused). */
+typedef enum sgemm_activation {
+    SGEMM_ACT_NONE = 0,
+    SGEMM_ACT_RELU = 1,      /* max(x, 0); NaN stays NaN */
+    SGEMM_ACT_GELU = 2,      /* 0.5 x (1 + erf(x / sqrt 2))  (Hendrycks & Gimpel 2016) */
+    SGEMM_ACT_GELU_TANH = 3, /* 0.5 x (1 + tanh(sqrt(2 / pi) (x + 0.044715 x^3))) */
+    SGEMM_ACT_SILU = 4       /* x / (1 + exp(-x))  (Elfwing, Uchibe & Doya 2018) */
+} sgemm_activation_t;
+
 /*
  * C = alpha * (A . B) + beta * C on the FP32 SIMT path ("GEMM scrapbook": 2D block tiling
  * with register outer products, float4 loads, warp tiling and double buffering; here a
@@ -192,6 +201,36 @@ sgemm_status_t sgemm_ex_strided_batched(sgemm_op_t transa, sgemm_op_t transb, sg
                                         const float *B, int64_t ldb, int64_t strideB,
                                         float beta, float *C, int64_t ldc, int64_t strideC,
                                         int64_t batch, void *stream);
+
+/*
+ * Fused epilogue for layer-shaped products ("GEMM scrapbook": a language model is mostly
+ * projections and feed-forward GEMMs; the bias, activation and residual around them are the
+ * BLAS-external part fused here):
+ *
+ *     C = act(alpha * op(A) . op(B) + bias) + beta * C
+ *
+ * bias: N floats added to every row (device pointer, shared by every batch entry), or NULL.
+ * act: applied after the bias and before the beta * C term, so act(x W + b) is beta = 0 and
+ * x W + b + residual is act = SGEMM_ACT_NONE with beta = 1 and C holding the residual. Every
+ * path, operand form and kernel applies the epilogue in registers before the single write of
+ * C; when alpha == 0 or K == 0 the result is act(bias) + beta * C. Arguments and errors are
+ * those of sgemm_ex / sgemm_ex_strided_batched; an unknown activation returns
+ * SGEMM_ERR_INVALID_VALUE. The activations use CUDA's erff / tanhf / expf.
+ */
+sgemm_status_t sgemm_fused(sgemm_op_t transa, sgemm_op_t transb, sgemm_path_t path,
+                           int64_t M, int64_t N, int64_t K, float alpha,
+                           const float *A, int64_t lda, const float *B, int64_t ldb,
+                           float beta, float *C, int64_t ldc, const float *bias,
+                           sgemm_activation_t act, void *stream);
+
+/* Batched form of sgemm_fused (one bias vector for all batch entries). */
+sgemm_status_t sgemm_fused_strided_batched(sgemm_op_t transa, sgemm_op_t transb,
+                                           sgemm_path_t path, int64_t M, int64_t N, int64_t K,
+                                           float alpha, const float *A, int64_t lda,
+                                           int64_t strideA, const float *B, int64_t ldb,
+                                           int64_t strideB, float beta, float *C, int64_t ldc,
+                                           int64_t strideC, int64_t batch, const float *bias,
+                                           sgemm_activation_t act, void *stream);
 
 /* Static text for a status code (never NULL). */
 const char *sgemm_status_string(sgemm_status_t status);

@@ -67,6 +67,9 @@ def _bind(lib):
     lib.sgemm_ref_absdot_ex_rows.argtypes = [i32, i32, i64, i64, i64, p, i64, p, i64, p, i64,
                                              p, i64]
     lib.sgemm_ref_absdot_ex_rows.restype = ctypes.c_int
+    lib.sgemm_ref_epilogue_rows.argtypes = [i32, i32, i64, i64, i64, f64, p, i64, p, i64, f64, p,
+                                            i64, p, i32, p, i64, p, i64]
+    lib.sgemm_ref_epilogue_rows.restype = ctypes.c_int
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
     return lib
@@ -123,6 +126,32 @@ def sgemm_ex(transa: bool, transb: bool, M: int, N: int, K: int, alpha: float, A
     st = lib.sgemm_ref_ex_rows(int(bool(transa)), int(bool(transb)), M, N, K, float(alpha),
                                _ptr(A), lda, _ptr(B), ldb, float(beta), _ptr(C), ldc, _ptr(idx),
                                0 if idx is None else len(idx), _ptr(out), max(N, 1))
+    if st != 0:
+        raise ValueError(f"oracle rejected the arguments (status {st})")
+    return out
+
+
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2, "gelu_tanh": 3, "silu": 4}
+
+
+def sgemm_epilogue(transa: bool, transb: bool, M: int, N: int, K: int, alpha: float,
+                   A: np.ndarray, lda: int, B: np.ndarray, ldb: int, beta: float,
+                   C: np.ndarray | None, ldc: int, bias: np.ndarray | None, act: str | int,
+                   rows=None, lib=None) -> np.ndarray:
+    """act(alpha * op(A) op(B) + bias) + beta * C, rounded once to fp32 (see sgemm_ref.c)."""
+    lib = lib or load()
+    A = _as_f32(A)
+    B = _as_f32(B)
+    C = None if C is None else _as_f32(C)
+    bias = None if bias is None else _as_f32(np.ascontiguousarray(bias))
+    code = ACTIVATIONS[act] if isinstance(act, str) else int(act)
+    idx = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    R = M if idx is None else len(idx)
+    out = np.empty((R, N), dtype=np.float32)
+    st = lib.sgemm_ref_epilogue_rows(int(bool(transa)), int(bool(transb)), M, N, K, float(alpha),
+                                     _ptr(A), lda, _ptr(B), ldb, float(beta), _ptr(C), ldc,
+                                     _ptr(bias), code, _ptr(idx), 0 if idx is None else len(idx),
+                                     _ptr(out), max(N, 1))
     if st != 0:
         raise ValueError(f"oracle rejected the arguments (status {st})")
     return out

@@ -203,7 +203,83 @@ int sgemm_ref_absdot_ex_rows(int transa, int transb, int64_t M, int64_t N, int64
     return ORACLE_OK;
 }
 
-/* Threads the two loops above use (OpenMP over result rows). */
+/*
+ * Activation functions of the fused epilogue, in fp64, from their published definitions:
+ *   0 identity;  1 ReLU, max(x, 0) (NaN stays NaN);
+ *   2 GELU, x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2))   (Hendrycks & Gimpel, 2016);
+ *   3 GELU, tanh form 0.5 x (1 + tanh(sqrt(2 / pi) (x + 0.044715 x^3)))  (same paper);
+ *   4 SiLU, x * sigmoid(x) = x / (1 + exp(-x))   (Elfwing, Uchibe & Doya, 2018).
+ */
+static double activation(double x, int act) {
+    switch (act) {
+        case 1: return x > 0.0 ? x : (x != x ? x : 0.0);
+        case 2: return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+        case 3: {
+            const double c = sqrt(2.0 / 3.14159265358979323846);
+            return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+        }
+        case 4: return x / (1.0 + exp(-x));
+        default: return x;
+    }
+}
+
+/*
+ * Fused epilogue: out[i][j] = fl32( act(alpha * S_ij + bias[j]) + beta * C[i][j] ), with S_ij
+ * the transposed-operand sum of sgemm_ref_ex_rows (fp64, ascending k), bias a length-N vector
+ * (NULL: no bias), act as above, and C read only when beta != 0. act codes outside 0..4 are
+ * rejected.
+ */
+int sgemm_ref_epilogue_rows(int transa, int transb, int64_t M, int64_t N, int64_t K,
+                            double alpha, const float *A, int64_t lda, const float *B,
+                            int64_t ldb, double beta, const float *C, int64_t ldc,
+                            const float *bias, int act, const int64_t *rows, int64_t nrows,
+                            float *out, int64_t ldo) {
+    if (act < 0 || act > 4) return ORACLE_BAD_ARGS;
+    if (M < 0 || N < 0 || K < 0) return ORACLE_BAD_ARGS;
+    const int64_t a_cols = transa ? M : K, b_cols = transb ? K : N;
+    if (lda < (a_cols > 1 ? a_cols : 1) || ldb < (b_cols > 1 ? b_cols : 1)) return ORACLE_BAD_ARGS;
+    if (ldc < (N > 1 ? N : 1) || ldo < (N > 1 ? N : 1)) return ORACLE_BAD_ARGS;
+    const int64_t R = rows ? nrows : M;
+    if (R < 0) return ORACLE_BAD_ARGS;
+    for (int64_t r = 0; rows && r < R; ++r)
+        if (rows[r] < 0 || rows[r] >= M) return ORACLE_BAD_ARGS;
+    if (R == 0 || N == 0) return ORACLE_OK;
+    int failed = 0;
+
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)N * sizeof(double));
+        if (!acc) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < R; ++r) {
+            if (!acc) continue;
+            const int64_t i = rows ? rows[r] : r;
+            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;
+            if (alpha != 0.0) {
+                for (int64_t k = 0; k < K; ++k) {
+                    const double a = (double)(transa ? A[k * lda + i] : A[i * lda + k]);
+                    for (int64_t j = 0; j < N; ++j)
+                        acc[j] += a * (double)(transb ? B[j * ldb + k] : B[k * ldb + j]);
+                }
+            }
+            float *orow = out + r * ldo;
+            for (int64_t j = 0; j < N; ++j) {
+                double v = (alpha != 0.0) ? alpha * acc[j] : 0.0;
+                if (bias) v += (double)bias[j];
+                v = activation(v, act);
+                if (beta != 0.0) v += beta * (double)C[i * ldc + j];
+                orow[j] = (float)v;
+            }
+        }
+        free(acc);
+    }
+    return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+/* Threads the loops above use (OpenMP over result rows). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -17,6 +17,8 @@ Sources of each pin:
   bits; the exact sum is representable, so one final rounding reproduces it.
 * transposes: stored transposes through the ex entry agree with the plain product on
   numpy-transposed copies, with exact rational brute force, and with identity products.
+* fused epilogue: each activation against its published formula evaluated with Python's
+  math module; bias and residual against exact integer sums; activation before residual.
 * brute force: exact rational arithmetic (fractions.Fraction) on tiny shapes, rounded once
   to fp32; the oracle may differ by at most one fp32 ulp (its fp64 sum rounds before the
   final rounding).
@@ -247,6 +249,52 @@ def pin_transposed_brute_force(lib):
     return True
 
 
+def pin_epilogue_activations(lib):
+    # Pass chosen values x through the product (A = diag(x), B = I) and compare the fused
+    # epilogue with each activation's formula evaluated by Python's math module, rounded to
+    # fp32: a separate implementation of the published definitions.
+    import math
+    xs = np.array([-6.0, -2.5, -1.0, -0.25, 0.0, 0.5, 1.0, 3.0, 7.5], np.float32)
+    n = len(xs)
+    A = np.diag(xs).astype(np.float32)
+    eye = np.eye(n, dtype=np.float32)
+    forms = {
+        "none": lambda x: x,
+        "relu": lambda x: max(x, 0.0),
+        "gelu": lambda x: 0.5 * x * (1.0 + math.erf(x / math.sqrt(2.0))),
+        "gelu_tanh": lambda x: 0.5 * x * (1.0 + math.tanh(math.sqrt(2.0 / math.pi) *
+                                                          (x + 0.044715 * x ** 3))),
+        "silu": lambda x: x / (1.0 + math.exp(-x)),
+    }
+    for act, f in forms.items():
+        out = oracle.sgemm_epilogue(False, False, n, n, n, 1.0, A, n, eye, n, 0.0, None, n,
+                                    None, act, lib=lib)
+        want = np.diag([np.float32(f(float(x))) for x in xs])
+        off = ~np.eye(n, dtype=bool)
+        if not (np.array_equal(np.diag(out), np.diag(want)) and
+                np.array_equal(out[off], np.full(off.sum(), np.float32(f(0.0))))):
+            return False
+    return True
+
+
+def pin_epilogue_bias_and_residual(lib):
+    # act = none: alpha * S + bias + beta * C on exact small integers equals the int64 sum.
+    M, N, K = 7, 9, 33
+    A, B, C = synth.small_int(M, K, 81), synth.small_int(K, N, 82), synth.small_int(M, N, 83)
+    bias = synth.small_int(1, N, 84).reshape(-1)
+    S = A.astype(np.int64) @ B.astype(np.int64)
+    want = (2 * S + bias.astype(np.int64)[None, :] + 3 * C.astype(np.int64)).astype(np.float32)
+    got = oracle.sgemm_epilogue(False, False, M, N, K, 2.0, A, K, B, N, 3.0, C, N, bias, "none",
+                                lib=lib)
+    if not np.array_equal(got, want):
+        return False
+    # relu is applied before the residual: relu(S + bias) + C
+    want = (np.maximum(S + bias.astype(np.int64)[None, :], 0) + C.astype(np.int64)).astype(np.float32)
+    got = oracle.sgemm_epilogue(False, False, M, N, K, 1.0, A, K, B, N, 1.0, C, N, bias, "relu",
+                                lib=lib)
+    return np.array_equal(got, want)
+
+
 PINS = {
     "identity": pin_identity,
     "permutation": pin_permutation,
@@ -260,4 +308,6 @@ PINS = {
     "transposed_identity": pin_transposed_identity,
     "transposed_against_plain": pin_transposed_against_plain,
     "transposed_brute_force": pin_transposed_brute_force,
+    "epilogue_activations": pin_epilogue_activations,
+    "epilogue_bias_and_residual": pin_epilogue_bias_and_residual,
 }

@@ -92,6 +92,13 @@ def test_ex_argument_rules(sgemm_lib):
         assert L.sgemm_ex(*args) == sgemm_lib.SGEMM_ERR_INVALID_VALUE
 
 
+def test_fused_rejects_unknown_activation(sgemm_lib):
+    L = sgemm_lib.lib()
+    args = (0, 0, 0, 8, 6, 4, 1.0, FAKE, 4, FAKE, 6, 0.0, FAKE, 6, None, 9, None)
+    assert L.sgemm_fused(*args) == sgemm_lib.SGEMM_ERR_INVALID_VALUE
+    assert "activation" in L.sgemm_last_error().decode()
+
+
 def test_invalid_batched_arguments(sgemm_lib):
     L = sgemm_lib.lib()
     base = [8, 8, 8, 1.0, FAKE, 8, 64, FAKE, 8, 64, 0.0, FAKE, 8, 64, 2, None]

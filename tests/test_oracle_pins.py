@@ -44,6 +44,11 @@ MUTANTS = {
                               "const double a = (double)(transa ? A[i * lda + k] : A[i * lda + k]);"),
     "ex_transposed_B_index": ("acc[j] += a * (double)(transb ? B[j * ldb + k] : B[k * ldb + j]);",
                               "acc[j] += a * (double)(transb ? B[k * ldb + j] : B[k * ldb + j]);"),
+    "epilogue_gelu_constant": ("return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
+                               "return 0.5 * x * (1.0 + erf(x / 2.0));"),
+    "epilogue_act_after_residual": ("                v = activation(v, act);\n                if (beta != 0.0) v += beta * (double)C[i * ldc + j];",
+                                    "                if (beta != 0.0) v += beta * (double)C[i * ldc + j];\n                v = activation(v, act);"),
+    "epilogue_bias_dropped": ("if (bias) v += (double)bias[j];", "(void)bias;"),
     "wrong_row_index": ("const int64_t i = rows ? rows[r] : r;\n            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;",
                         "const int64_t i = r;\n            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;"),
 }
