@@ -26,6 +26,7 @@
 //    C never read when beta == 0.
 #include "epilogue.cuh"
 #include "ptx.cuh"
+#include "raster.cuh"
 #include "simt_gemm.cuh"
 #include "skinny_gemm.cuh"
 
@@ -55,19 +56,6 @@ struct KParams {
     const float *bias;  // fused epilogue (nullptr: none)
     int act;            // fused epilogue activation (0: none)
 };
-
-// Grouped raster order: GROUP_M consecutive tile rows are swept column by column, so CTAs
-// that run at the same time share A row panels and B column panels in L2.
-__device__ __forceinline__ void tile_coords(int pid, int tiles_m, int tiles_n, int group_m,
-                                            int &tm, int &tn) {
-    const int width = group_m * tiles_n;
-    const int group = pid / width;
-    const int first_m = group * group_m;
-    const int gsize = min(tiles_m - first_m, group_m);
-    const int in = pid - group * width;
-    tm = first_m + in % gsize;
-    tn = in / gsize;
-}
 
 // One k-tile (32 k-steps) of outer products for one thread's 8 x 16 tile.
 //   a_base: sA + (wm0 + tr) * 32, row r of the thread tile is 8 * r rows further (256 floats).

@@ -33,6 +33,7 @@
 // u = 2^-11, so the result carries TF32 rather than fp32 accuracy.
 #include "epilogue.cuh"
 #include "ptx.cuh"
+#include "raster.cuh"
 #include "tf32x3_gemm.cuh"
 
 #include <algorithm>
@@ -222,7 +223,7 @@ struct TParams {
     float *C;
     long long ldc, sC;
     int batch;
-    int tiles_m, tiles_n;
+    int tiles_m, tiles_n, group_m;
     int c_vec4;
     const float *bias;  // fused epilogue (nullptr: none)
     int act;            // fused epilogue activation (0: none)
@@ -255,7 +256,8 @@ __global__ void __launch_bounds__(192, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, b = blockIdx.y;
-    const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+    int tm, tn;  // grouped raster: a wave's A and B panels stay in L2
+    tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     const int m0 = tm * BM, n0 = tn * BN;
     const int KB = (p.K + BK - 1) / BK;
 
@@ -592,6 +594,7 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
     tp.batch = p.batch;
     tp.tiles_m = (p.M + BM - 1) / BM;
     tp.tiles_n = (p.N + BN - 1) / BN;
+    tp.group_m = 16;
     tp.c_vec4 = aligned16(p.C) && p.ldc % 4 == 0 && (p.batch <= 1 || p.strideC % 4 == 0);
     tp.bias = p.bias;
     tp.act = p.act;
