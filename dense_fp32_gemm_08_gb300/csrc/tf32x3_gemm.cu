@@ -37,6 +37,7 @@
 #include "tf32x3_gemm.cuh"
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -610,15 +611,36 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
     return err;
 }
 
+// Tile width of the tensor paths. Measured on a GB300 (TFLOP/s, fp32-equivalent):
+//   1xTF32  4096^3: N=128 421, N=256 535;  16384x12288x4096: N=128 461, N=256 654
+//   3xTF32  4096^3: N=128 241, N=256 217;  16384x12288x4096: N=128 266, N=256 270
+// N = 256 halves the A operand's shared-memory reads per unit of MMA work, which is what
+// bounds these kernels; 3xTF32 at N = 256 has only two stages and fewer, larger tiles, so it
+// wins only once the grid is several waves deep. SGEMM_TF32_TILE_N=128|256 forces a width.
+int tensor_tile_n(const SimtProblem &p, bool three_products) {
+    static const int forced = [] {
+        const char *env = std::getenv("SGEMM_TF32_TILE_N");
+        if (env && std::strcmp(env, "256") == 0) return 256;
+        if (env && std::strcmp(env, "128") == 0) return 128;
+        return 0;
+    }();
+    if (forced) return forced;
+    if (!three_products) return 256;
+    const long long tiles256 = static_cast<long long>((p.M + BM - 1) / BM) * ((p.N + 255) / 256) * p.batch;
+    return tiles256 >= 6LL * 152 ? 256 : 128;
+}
+
 }  // namespace
 
 bool tf32x3_supports(const SimtProblem &p) { return p.batch <= 65535; }
 
 cudaError_t tf32x3_launch(const SimtProblem &p, cudaStream_t stream, const char **detail) {
+    if (tensor_tile_n(p, true) == 256) return launch_tf32x3<256, 2, 2, 3>(p, stream, detail);
     return launch_tf32x3<128, 3, 4, 3>(p, stream, detail);
 }
 
 cudaError_t tf32_launch(const SimtProblem &p, cudaStream_t stream, const char **detail) {
+    if (tensor_tile_n(p, false) == 256) return launch_tf32x3<256, 4, 2, 1>(p, stream, detail);
     return launch_tf32x3<128, 6, 4, 1>(p, stream, detail);
 }
 
