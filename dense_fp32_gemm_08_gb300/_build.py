@@ -35,7 +35,8 @@ def _sources() -> list[Path]:
 
 def _inputs() -> list[Path]:
     return _sources() + sorted(CSRC.glob("*.cuh")) + sorted(CSRC.glob("*.h")) + \
-        sorted(INCLUDE.glob("*.h")) + [Path(__file__)]
+        sorted(INCLUDE.glob("*.h")) + [Path(__file__)] + sorted((PKG / "tuning").glob("*.py")) + \
+        sorted((PKG / "tuning").glob("*.json"))
 
 
 def is_stale() -> bool:
@@ -55,8 +56,17 @@ def _compile(src: Path) -> tuple[Path, str]:
     return obj, proc.stderr
 
 
+def generate_sources() -> None:
+    """Write csrc/config_table_gen.h from the measured tuning data."""
+    if str(ROOT) not in sys.path:
+        sys.path.insert(0, str(ROOT))
+    from dense_fp32_gemm_08_gb300.tuning import gen_table
+    gen_table.generate()
+
+
 def build(force: bool = False, verbose: bool = False) -> Path:
     """Compile and link the library; returns its path."""
+    generate_sources()
     if not force and not is_stale():
         return LIBRARY
     BUILD_DIR.mkdir(exist_ok=True)

@@ -1,7 +1,8 @@
 // config_table.h: per-shape-class choice of SIMT kernel configuration.
 //
-// The classes and their winners come from device-timed sweeps on a GB300 (152 SMs), one
-// configuration forced at a time (bench.py with SGEMM_FORCE_CONFIG):
+// The winner of each shape class is measured (tuning/sweep.py) and written into
+// config_table_gen.h by tuning/gen_table.py at build time. Earlier hand sweeps that shaped the
+// classes (bench.py with SGEMM_FORCE_CONFIG, one configuration at a time, GB300, 152 SMs):
 //
 //   class                       measured                                         choice
 //   aligned, <  6 waves of       4096^3: sk 128x256 63.6 TF/s, dp 128x128 62.0,   sk_tma_ws_128x256_s4
@@ -19,6 +20,7 @@
 //   M <= 8 (any alignment)       1x4096x4096: tile kernels 0.34 ms (HBM-bound)     skinny_wide_m8
 #pragma once
 
+#include "config_table_gen.h"
 #include "simt_gemm.cuh"
 
 namespace sg {
@@ -42,28 +44,56 @@ enum : int {
     kCfgPackedDp128x128 = 15,
 };
 
+// Shape classes, in the order of kClassWinner (config_table_gen.h) and of
+// tuning/classes.py, which defines the same rule.
+enum ShapeClass : int {
+    kAlignedTiny = 0,
+    kAlignedSmall,
+    kAlignedMedium,
+    kAlignedLarge,
+    kUnalignedTiny,
+    kUnalignedSmall,
+    kUnalignedMedium,
+    kUnalignedLarge,
+};
+
 // Waves of 128 x 128 tiles at two CTAs per SM on a 152-SM part.
 inline double waves_128x128(const SimtProblem &p) {
     const double tiles = static_cast<double>((p.M + 127) / 128) * ((p.N + 127) / 128) * p.batch;
     return tiles / (2.0 * 152.0);
 }
 
-// Picks the configuration id for a problem from its shape class and operand alignment.
+inline int shape_class(const SimtProblem &p, bool aligned) {
+    const int base = aligned ? kAlignedTiny : kUnalignedTiny;
+    if (static_cast<long long>(p.M) * p.N * p.batch <= 128LL * 128) return base;
+    const double w = waves_128x128(p);
+    return base + (w < 1.0 ? 1 : w < 6.0 ? 2 : 3);
+}
+
+inline int config_by_name(const char *name) {
+    for (int i = 0; i < simt_num_configs(); ++i) {
+        const char *a = simt_config(i).name;
+        int j = 0;
+        while (a[j] && a[j] == name[j]) ++j;
+        if (a[j] == name[j]) return i;
+    }
+    return -1;
+}
+
+// Picks the configuration id for a problem: the bandwidth kernels for skinny shapes, else
+// the measured winner of the problem's shape class (falling back to a configuration that
+// can run the problem when the winner cannot, e.g. a broadcast batch that cannot be
+// repacked).
 inline int table_choose(const SimtProblem &p) {
     // One output dimension of at most 8: HBM-bound, the bandwidth kernels (any alignment).
     if (simt_config_supports(kCfgSkinnyTall, p)) return kCfgSkinnyTall;
     if (simt_config_supports(kCfgSkinnyWide, p)) return kCfgSkinnyWide;
     const bool tma = simt_config_supports(kCfgDpTma128x128, p);
-    const double waves = waves_128x128(p);
-    const bool tiny = static_cast<long long>(p.M) * p.N * p.batch <= 128LL * 128;
-    if (!tma) {
-        if (simt_config_supports(kCfgPackedSk128x256, p))
-            return waves >= 6.0 ? kCfgPackedDp128x128 : kCfgPackedSk128x256;
-        return waves >= 6.0 ? kCfgDpCp128x128 : kCfgSkCp128x256;
-    }
-    if (tiny) return kCfgDpTma128x128;
-    if (waves >= 6.0) return kCfgDpTma128x128;
-    return kCfgSkTma128x256;
+    const int cls = shape_class(p, tma);
+    const int id = config_by_name(kClassWinner[cls]);
+    if (id >= 0 && simt_config_supports(id, p)) return id;
+    if (tma) return kCfgSkTma128x256;
+    return waves_128x128(p) >= 6.0 ? kCfgDpCp128x128 : kCfgSkCp128x256;
 }
 
 }  // namespace sg

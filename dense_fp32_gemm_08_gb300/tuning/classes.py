@@ -1,0 +1,44 @@
+"""Shape classes of the configuration table, their representative shapes and candidates.
+
+A class is decided by the operands' TMA alignment and by the grid depth in waves of 128 x 128
+tiles at two CTAs per SM (152 SMs): the same rule `config_table.h` applies at run time.
+The M <= 8 and N <= 8 shapes always take the bandwidth kernels and are not swept."""
+from __future__ import annotations
+
+SMS = 152
+
+# class name -> (representative (M, N, K) shapes, candidate configuration names)
+ALIGNED = ["dp_tma_128x128_s3", "dp_tma_128x256_s4", "sk_tma_ws_128x256_s4",
+           "sk_tma_ws_256x128_s4", "pdp_tma_ws_128x256_s4"]
+UNALIGNED = ["packed_sk_tma_128x256_s4", "packed_dp_tma_128x128_s3", "sk_cpasync_128x256_s4",
+             "dp_cpasync_128x256_s4", "dp_cpasync_128x128_s3"]
+
+CLASSES = {
+    "aligned_tiny": ([(96, 96, 512), (128, 64, 2048)], ALIGNED),
+    "aligned_small": ([(512, 512, 512), (1024, 1024, 1024), (2048, 2048, 2048)], ALIGNED),
+    "aligned_medium": ([(4096, 4096, 4096), (4096, 3072, 2048), (3072, 4096, 4096)], ALIGNED),
+    "aligned_large": ([(8192, 8192, 8192), (16384, 12288, 4096)], ALIGNED),
+    "unaligned_tiny": ([(97, 95, 513), (127, 129, 4099)], UNALIGNED),
+    "unaligned_small": ([(1001, 999, 1003), (2047, 2045, 2049)], UNALIGNED),
+    "unaligned_medium": ([(4095, 3001, 1537), (4097, 4093, 4099)], UNALIGNED),
+    "unaligned_large": ([(8191, 8193, 8195)], UNALIGNED),
+}
+
+CLASS_ORDER = list(CLASSES)
+
+
+def waves(M: int, N: int, batch: int = 1) -> float:
+    return ((M + 127) // 128) * ((N + 127) // 128) * batch / (2.0 * SMS)
+
+
+def classify(M: int, N: int, aligned: bool, batch: int = 1) -> str:
+    """The class of a problem (mirrors table_choose in config_table.h)."""
+    prefix = "aligned" if aligned else "unaligned"
+    if M * N * batch <= 128 * 128:
+        return prefix + "_tiny"
+    w = waves(M, N, batch)
+    if w < 1.0:
+        return prefix + "_small"
+    if w < 6.0:
+        return prefix + "_medium"
+    return prefix + "_large"
