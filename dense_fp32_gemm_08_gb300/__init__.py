@@ -17,7 +17,8 @@ from pathlib import Path
 __all__ = [
     "SgemmError", "library_path", "lib", "sgemm", "sgemm_strided_batched", "sgemm_3xtf32",
     "sgemm_3xtf32_strided_batched", "sgemm_tf32", "sgemm_tf32_strided_batched", "sgemm_ex",
-    "sgemm_ex_strided_batched", "sgemm_fused", "sgemm_fused_strided_batched", "sgemm_noalloc", "sgemm_status_string", "sgemm_last_error",
+    "sgemm_ex_strided_batched", "sgemm_fused", "sgemm_fused_strided_batched", "sgemm_host",
+    "sgemm_noalloc", "sgemm_status_string", "sgemm_last_error",
     "sgemm_device_status", "sgemm_release_workspace", "sgemm_num_configs",
     "sgemm_config_name", "sgemm_select_config", "sgemm_force_config",
     "sgemm_selftest_bounded_wait", "matmul",
@@ -66,6 +67,7 @@ def _bind(L):
     gemm = [i64, i64, i64, f32, p, i64, p, i64, f32, p, i64, p]
     batched = [i64, i64, i64, f32, p, i64, i64, p, i64, i64, f32, p, i64, i64, i64, p]
     for name, args in (("sgemm", gemm), ("sgemm_3xtf32", gemm), ("sgemm_noalloc", gemm),
+                       ("sgemm_host", gemm),
                        ("sgemm_tf32", gemm), ("sgemm_strided_batched", batched),
                        ("sgemm_3xtf32_strided_batched", batched),
                        ("sgemm_tf32_strided_batched", batched)):
@@ -221,6 +223,29 @@ def sgemm_fused_strided_batched(transa, transb, M, N, K, alpha, A, lda, strideA,
                                              _ptr(A), lda, strideA, _ptr(B), ldb, strideB, beta,
                                              _ptr(C), ldc, strideC, batch, _ptr(bias), code,
                                              _stream(stream)))
+
+
+def _host_ptr(x):
+    if x is None or isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):  # a CPU torch tensor (pinned or not)
+        if x.is_cuda:
+            raise TypeError("sgemm_host takes host tensors")
+        if str(x.dtype) != "torch.float32":
+            raise TypeError("tensor arguments must be float32")
+        return x.data_ptr()
+    import numpy as np
+    a = x if isinstance(x, np.ndarray) else np.asarray(x)
+    if a.dtype != np.float32:
+        raise TypeError("arrays must be float32")
+    return a.ctypes.data
+
+
+def sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:
+    """C = alpha * A.B + beta * C with host-memory operands (numpy arrays, CPU tensors or
+    addresses); returns when C holds the result. Pinned memory lets copies overlap compute."""
+    _check(lib().sgemm_host(M, N, K, alpha, _host_ptr(A), lda, _host_ptr(B), ldb, beta,
+                            _host_ptr(C), ldc, _stream(stream)))
 
 
 def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:

@@ -9,6 +9,7 @@
 
 #include "config_table.h"
 #include "epilogue.cuh"
+#include "host_gemm.cuh"
 #include "ptx.cuh"
 #include "simt_gemm.cuh"
 #include "tf32x3_gemm.cuh"
@@ -213,6 +214,19 @@ sgemm_status_t dispatch(const Args &a, void *stream_ptr, Path path) {
     return path == kPathSimt ? run_simt(a, stream) : run_tensor(a, stream, path);
 }
 
+// Device product used by each chunk of the host-memory path (the SIMT path).
+cudaError_t chunk_gemm(long long M, long long N, long long K, float alpha, const float *A,
+                       long long lda, const float *B, long long ldb, float beta, float *C,
+                       long long ldc, cudaStream_t stream, const char **detail) {
+    Args a{M, N, K, alpha, beta, A, lda, 0, B, ldb, 0, C, ldc, 0, 1};
+    const sgemm_status_t st = (alpha == 0.0f || K == 0) ? run_scale(a, stream) : run_simt(a, stream);
+    if (st != SGEMM_OK) {
+        *detail = "a chunk's device product failed";
+        return cudaErrorLaunchFailure;
+    }
+    return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -361,6 +375,27 @@ sgemm_status_t sgemm_ex(sgemm_op_t transa, sgemm_op_t transb, sgemm_path_t path,
                                     beta, C, ldc, 0, 1, stream);
 }
 
+sgemm_status_t sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                          int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                          int64_t ldc, void *stream_ptr) {
+    Args a{M, N, K, alpha, beta, A, lda, 0, B, ldb, 0, C, ldc, 0, 1};
+    t_last_error[0] = '\0';
+    sgemm_status_t st = validate(a);
+    if (st != SGEMM_OK) return st;
+    if (is_noop(a)) return SGEMM_OK;
+    st = check_limits(a);
+    if (st != SGEMM_OK) return st;
+    if (!have_device()) return fail(SGEMM_ERR_UNSUPPORTED, "no CUDA device available");
+    const sg::HostProblem hp{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
+    const char *detail = "";
+    cudaError_t err = sg::host_gemm(hp, static_cast<cudaStream_t>(stream_ptr), chunk_gemm, &detail);
+    if (err != cudaSuccess) {
+        if (t_last_error[0] != '\0') return SGEMM_ERR_LAUNCH;  // the chunk's own message stands
+        return fail_cuda(detail, err);
+    }
+    return SGEMM_OK;
+}
+
 const char *sgemm_status_string(sgemm_status_t status) {
     switch (status) {
         case SGEMM_OK: return "SGEMM_OK";
@@ -393,6 +428,8 @@ sgemm_status_t sgemm_release_workspace(void) {
     if (err != cudaSuccess) return fail_cuda("device synchronize", err);
     err = sg::release_workspaces();
     cudaError_t err3 = sg::release_pack_workspaces();
+    cudaError_t err4 = sg::release_host_buffers();
+    if (err3 == cudaSuccess) err3 = err4;
     cudaError_t err2 = sg::tf32x3_release_workspaces();
     if (err == cudaSuccess) err = err3;
     if (err != cudaSuccess) return fail_cuda("workspace free", err);

@@ -234,6 +234,21 @@ sgemm_status_t sgemm_fused_strided_batched(sgemm_op_t transa, sgemm_op_t transb,
                                            int64_t strideC, int64_t batch, const float *bias,
                                            sgemm_activation_t act, void *stream);
 
+/*
+ * The product with A, B and C in HOST memory (same sizes, leading dimensions, alpha / beta
+ * rules and argument errors as sgemm()). The call returns when C holds the result. B is
+ * uploaded once; the rows of A (and of C when beta != 0) travel in chunks of about M / 8
+ * rows through two device buffers each, uploaded on an internal stream while the previous
+ * chunk is computed on `stream` (the SIMT path) and the one before it is downloaded on
+ * another internal stream. With pinned (page-locked) host memory the copies overlap the
+ * computation; pageable memory works but the copies then serialise. Device buffers of
+ * 4 * (K * N + 2 * chunk * (K + N)) bytes are kept per device until
+ * sgemm_release_workspace(); calls on the same device run one at a time.
+ */
+sgemm_status_t sgemm_host(int64_t M, int64_t N, int64_t K, float alpha,
+                          const float *A, int64_t lda, const float *B, int64_t ldb,
+                          float beta, float *C, int64_t ldc, void *stream);
+
 /* Static text for a status code (never NULL). */
 const char *sgemm_status_string(sgemm_status_t status);
 
