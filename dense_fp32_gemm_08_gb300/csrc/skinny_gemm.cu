@@ -7,8 +7,9 @@
 //   float4 (or scalar) chunks of the row, multiplies them by the matching rows of B (K x N,
 //   small and L1/L2-resident), and keeps N partial sums; a shuffle tree in fixed lane order
 //   reduces them. Every row is independent; M rows give M warps of work.
-// * M <= 8 ("wide"): the large operand is B (K x N). A CTA of 8 warps owns 128 columns of C;
-//   its 8-CTA cluster splits K into 8 ranges, and within a CTA warp w takes k = w, w + 8, ...
+// * M <= 8 ("wide"): the large operand is B (K x N). A CTA of 16 warps (8 when M > 4) owns
+//   128 columns of C; its 8-CTA cluster splits K into 8 ranges, and within a CTA warp w takes
+//   k = w, w + 16, ... (w, w + 8, ...)
 //   of its range, so every warp streams whole 512-byte row segments of B. Partial sums are
 //   reduced over the warps through shared memory and over the cluster through distributed
 //   shared memory, both in a fixed order; the cluster's CTA 0 applies alpha / beta. No
@@ -42,19 +43,36 @@ __global__ void __launch_bounds__(256) skinny_tall_kernel(SkinnyProblem p) {
         for (int n = 0; n < NN; ++n) acc[n] = 0.0f;
         int k = 0;
         if (VEC) {
-            // 4 k-values per lane per step, 128 per warp, unrolled for loads in flight.
+            // 4 k-values per lane per step, 128 per warp, unrolled for loads in flight; each
+            // lane adds its own k-values in ascending order. With N == 1 and B a packed,
+            // aligned vector, B's four values come in one float4 as well.
             const int kv = p.K & ~127;
+            const bool bvec = NN == 1 && p.ldb == 1 &&
+                              (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
+            if (bvec) {
 #pragma unroll 4
-            for (int k0 = 0; k0 < kv; k0 += 128) {
-                const int kk = k0 + 4 * lane;
-                const float4 av = __ldcs(reinterpret_cast<const float4 *>(a + kk));
-                const float ae[4] = {av.x, av.y, av.z, av.w};
+                for (int k0 = 0; k0 < kv; k0 += 128) {
+                    const int kk = k0 + 4 * lane;
+                    const float4 av = __ldcs(reinterpret_cast<const float4 *>(a + kk));
+                    const float4 bv = __ldg(reinterpret_cast<const float4 *>(B + kk));
+                    acc[0] = fmaf(av.x, bv.x, acc[0]);
+                    acc[0] = fmaf(av.y, bv.y, acc[0]);
+                    acc[0] = fmaf(av.z, bv.z, acc[0]);
+                    acc[0] = fmaf(av.w, bv.w, acc[0]);
+                }
+            } else {
+#pragma unroll 4
+                for (int k0 = 0; k0 < kv; k0 += 128) {
+                    const int kk = k0 + 4 * lane;
+                    const float4 av = __ldcs(reinterpret_cast<const float4 *>(a + kk));
+                    const float ae[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float *brow = B + static_cast<long long>(kk + e) * p.ldb;
+                    for (int e = 0; e < 4; ++e) {
+                        const float *brow = B + static_cast<long long>(kk + e) * p.ldb;
 #pragma unroll
-                    for (int n = 0; n < NN; ++n)
-                        if (n < p.N) acc[n] = fmaf(ae[e], __ldg(brow + n), acc[n]);
+                        for (int n = 0; n < NN; ++n)
+                            if (n < p.N) acc[n] = fmaf(ae[e], __ldg(brow + n), acc[n]);
+                    }
                 }
             }
             k = kv;
@@ -85,12 +103,17 @@ __global__ void __launch_bounds__(256) skinny_tall_kernel(SkinnyProblem p) {
 // ---- wide: M <= 8 --------------------------------------------------------------------------------
 
 constexpr int kWideCols = 128;   // columns of C per CTA (32 lanes x float4)
-constexpr int kWideWarps = 8;
 constexpr int kCluster = 8;      // CTAs per cluster, splitting K
 
+// Warps per CTA: as many as the reduction buffer allows (16 up to four rows, 8 for eight), so
+// that enough row segments of B are in flight to keep HBM busy.
+template <int MM>
+__host__ __device__ constexpr int wide_warps() { return MM <= 4 ? 16 : 8; }
+
 template <int MM, bool VEC>
-__global__ void __cluster_dims__(1, kCluster, 1) __launch_bounds__(kWideWarps * 32)
+__global__ void __cluster_dims__(1, kCluster, 1) __launch_bounds__(wide_warps<MM>() * 32)
     skinny_wide_kernel(SkinnyProblem p) {
+    constexpr int kWideWarps = wide_warps<MM>();
     __shared__ float4 part[kWideWarps][MM][32];
     cg::cluster_group cluster = cg::this_cluster();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -193,10 +216,11 @@ template <int MM>
 cudaError_t launch_wide(const SkinnyProblem &p, cudaStream_t stream) {
     const bool vec = aligned16(p.B) && p.ldb % 4 == 0 && (p.batch <= 1 || p.strideB % 4 == 0);
     dim3 grid((p.N + kWideCols - 1) / kWideCols, kCluster, p.batch);
+    constexpr int threads = wide_warps<MM>() * 32;
     if (vec)
-        skinny_wide_kernel<MM, true><<<grid, kWideWarps * 32, 0, stream>>>(p);
+        skinny_wide_kernel<MM, true><<<grid, threads, 0, stream>>>(p);
     else
-        skinny_wide_kernel<MM, false><<<grid, kWideWarps * 32, 0, stream>>>(p);
+        skinny_wide_kernel<MM, false><<<grid, threads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
