@@ -42,6 +42,8 @@ enum : int {
     kCfgSkCp256x128 = 13,
     kCfgPackedSk128x256 = 14,
     kCfgPackedDp128x128 = 15,
+    kCfgSkTma128x256k64 = 16,
+    kCfgSkTma256x128k64 = 17,
 };
 
 // Shape classes, in the order of kClassWinner (config_table_gen.h) and of

@@ -448,16 +448,20 @@ struct TmaProducer {
 
 // MAXREG caps registers per thread: four-warp tiles run two CTAs per SM and must leave room
 // for both in the register file.
+// KSUB: 32-wide k sub-tiles per pipeline stage (a stage then covers 32 * KSUB values of k,
+// with one CTA barrier and one TMA refill per stage); the TMA loader only for KSUB > 1.
 template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG,
-          int LOADER = kLoaderTma>
+          int LOADER = kLoaderTma, int KSUB = 1>
 __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
     simt_gemm_persistent_kernel(const __grid_constant__ CUtensorMap mapA,
                                 const __grid_constant__ CUtensorMap mapB, const PParams p) {
     constexpr int WARPS = WARPS_M * WARPS_N;
     static_assert(BM == WARPS_M * 64 && BN == WARPS_N * 64, "64 x 64 warp tiles");
     static_assert(STAGES >= 2, "at least double buffering");
-    constexpr int A_FLOATS = BM * BK;
-    constexpr int STAGE_FLOATS = A_FLOATS + BK * BN;
+    static_assert(KSUB == 1 || LOADER == kLoaderTma, "wide stages with the TMA loader only");
+    constexpr int A_SUB = BM * BK;          // one 32-wide A sub-tile
+    constexpr int A_FLOATS = KSUB * A_SUB;  // B follows the A sub-tiles
+    constexpr int STAGE_FLOATS = A_FLOATS + KSUB * BK * BN;
     constexpr uint32_t STAGE_BYTES = STAGE_FLOATS * 4;
 
     extern __shared__ uint8_t smem_raw[];
@@ -493,8 +497,11 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
         float *sA = smem + s * STAGE_FLOATS;
         if (LOADER == kLoaderTma) {
             mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-            tma_load_3d(sA, &mapA, &full[s], prod.kt * BK, prod.m0, prod.b);
-            tma_load_3d(sA + A_FLOATS, &mapB, &full[s], prod.n0, prod.kt * BK, prod.b);
+#pragma unroll
+            for (int j = 0; j < KSUB; ++j)
+                tma_load_3d(sA + j * A_SUB, &mapA, &full[s], (prod.kt * KSUB + j) * BK, prod.m0,
+                            prod.b);
+            tma_load_3d(sA + A_FLOATS, &mapB, &full[s], prod.n0, prod.kt * KSUB * BK, prod.b);
         } else {
             cp_async_stage<BM, BN, WARPS * 32>(
                 sA, sA + A_FLOATS, p.k, p.k.A + static_cast<long long>(prod.b) * p.k.sA,
@@ -539,7 +546,10 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
                 cp_async_commit();
             }
             const float *sA = smem + s * STAGE_FLOATS;
-            compute_ktile<BN>(sA + (wm0 + tr) * BK, tr, sA + A_FLOATS + wn0 + 4 * tc, acc);
+#pragma unroll
+            for (int j = 0; j < KSUB; ++j)
+                compute_ktile<BN>(sA + j * A_SUB + (wm0 + tr) * BK, tr,
+                                  sA + A_FLOATS + j * BK * BN + wn0 + 4 * tc, acc);
             if (LOADER == kLoaderTma) {
                 __syncthreads();  // every warp is done with stage s
                 if (s_abort) break;
@@ -675,6 +685,8 @@ const SimtConfig kConfigs[] = {
     {"sk_cpasync_256x128_s4", 256, 128, 4, 2, 4, kLoaderCpAsync, kScheduleStreamK},
     {"packed_sk_tma_128x256_s4", 128, 256, 2, 4, 4, kLoaderTma, kScheduleStreamK},
     {"packed_dp_tma_128x128_s3", 128, 128, 2, 2, 3, kLoaderTma, kScheduleDataParallel},
+    {"sk_tma_ws_128x256_k64_s2", 128, 256, 2, 4, 2, kLoaderTma, kScheduleStreamK},
+    {"sk_tma_ws_256x128_k64_s2", 256, 128, 4, 2, 2, kLoaderTma, kScheduleStreamK},
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 
@@ -822,14 +834,15 @@ int device_sms(int dev) {
 constexpr int kMinItersPerCta = 4;
 
 template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG = 255,
-          int LOADER = kLoaderTma>
+          int LOADER = kLoaderTma, int KSUB = 1>
 cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t stream,
                               const char **detail) {
     constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
     constexpr int THREADS = CONSUMER_WARPS * 32;
-    constexpr size_t SMEM = static_cast<size_t>(STAGES) * (BM * BK + BK * BN) * 4 +
+    constexpr size_t SMEM = static_cast<size_t>(STAGES) * KSUB * (BM * BK + BK * BN) * 4 +
                             2 * STAGES * sizeof(uint64_t) + 1024;
-    auto kernel = simt_gemm_persistent_kernel<BM, BN, WARPS_M, WARPS_N, STAGES, MAXREG, LOADER>;
+    auto kernel =
+        simt_gemm_persistent_kernel<BM, BN, WARPS_M, WARPS_N, STAGES, MAXREG, LOADER, KSUB>;
 
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -893,7 +906,7 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
         *detail = "too many output tiles";
         return cudaErrorInvalidValue;
     }
-    const int KT = (p.K + BK - 1) / BK;
+    const int KT = (p.K + BK * KSUB - 1) / (BK * KSUB);  // k-tiles of the stage width
     const long long g_full = static_cast<long long>(sms) * occupancy[dev];
     long long dp_tiles = T, G = T < g_full ? T : g_full;
     if (schedule == kScheduleStreamK && T % g_full != 0) {
@@ -938,7 +951,7 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
     memset(&mapB, 0, sizeof(mapB));
     if (LOADER == kLoaderTma &&
         (!make_map(&mapA, p.A, p.M, p.K, p.lda, p.strideA, p.batch, BM, BK, true) ||
-         !make_map(&mapB, p.B, p.K, p.N, p.ldb, p.strideB, p.batch, BK, BN, false))) {
+         !make_map(&mapB, p.B, p.K, p.N, p.ldb, p.strideB, p.batch, BK * KSUB, BN, false))) {
         *detail = "cuTensorMapEncodeTiled rejected an operand";
         return cudaErrorInvalidValue;
     }
@@ -994,6 +1007,12 @@ cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const
                                                                             stream, detail);
         case 14: return launch_packed(5, p, stream, detail);
         case 15: return launch_packed(2, p, stream, detail);
+        case 16:
+            return launch_persistent<128, 256, 2, 4, 2, 255, kLoaderTma, 2>(kScheduleStreamK, p,
+                                                                           stream, detail);
+        case 17:
+            return launch_persistent<256, 128, 4, 2, 2, 255, kLoaderTma, 2>(kScheduleStreamK, p,
+                                                                           stream, detail);
         default: *detail = "unknown SIMT configuration"; return cudaErrorInvalidValue;
     }
 }

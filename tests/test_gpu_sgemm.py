@@ -154,7 +154,7 @@ def test_skinny_strided_batched(sg, M, N, K, batch):
 
 # ---- every configuration of the table ---------------------------------------------------------
 
-@pytest.mark.parametrize("cfg", range(16))
+@pytest.mark.parametrize("cfg", range(20))
 @pytest.mark.parametrize("shape", [(640, 768, 544), (257, 383, 129), (128, 256, 32),
                                    (4096, 2560, 320), (1000, 3000, 2000)])
 def test_each_config(sg, cfg, shape):
@@ -172,7 +172,8 @@ def test_each_config(sg, cfg, shape):
 
 @pytest.mark.parametrize("name", ["sk_tma_ws_128x256_s4", "sk_tma_ws_256x128_s4",
                                   "sk_tma_ws_128x128_s3", "sk_cpasync_128x256_s4",
-                                  "sk_cpasync_256x128_s4", "packed_sk_tma_128x256_s4"])
+                                  "sk_cpasync_256x128_s4", "packed_sk_tma_128x256_s4",
+                                  "sk_tma_ws_128x256_k64_s2", "sk_tma_ws_256x128_k64_s2"])
 def test_stream_k_deterministic_and_exact(sg, name):
     ids = {sg.sgemm_config_name(i): i for i in range(sg.sgemm_num_configs())}
     sg.sgemm_force_config(ids[name])
