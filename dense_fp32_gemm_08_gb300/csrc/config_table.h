@@ -44,6 +44,7 @@ enum : int {
     kCfgPackedDp128x128 = 15,
     kCfgSkTma128x256k64 = 16,
     kCfgSkTma256x128k64 = 17,
+    kCfgPackedSk256x128k64 = 18,
 };
 
 // Shape classes, in the order of kClassWinner (config_table_gen.h) and of

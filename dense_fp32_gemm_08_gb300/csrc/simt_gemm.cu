@@ -446,8 +446,7 @@ struct TmaProducer {
     }
 };
 
-// MAXREG caps registers per thread: four-warp tiles run two CTAs per SM and must leave room
-// for both in the register file.
+// MAXREG caps registers per thread (255 leaves room for two four-warp CTAs per SM).
 // KSUB: 32-wide k sub-tiles per pipeline stage (a stage then covers 32 * KSUB values of k,
 // with one CTA barrier and one TMA refill per stage); the TMA loader only for KSUB > 1.
 template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG,
@@ -687,6 +686,7 @@ const SimtConfig kConfigs[] = {
     {"packed_dp_tma_128x128_s3", 128, 128, 2, 2, 3, kLoaderTma, kScheduleDataParallel},
     {"sk_tma_ws_128x256_k64_s2", 128, 256, 2, 4, 2, kLoaderTma, kScheduleStreamK},
     {"sk_tma_ws_256x128_k64_s2", 256, 128, 4, 2, 2, kLoaderTma, kScheduleStreamK},
+    {"packed_sk_tma_256x128_k64_s2", 256, 128, 4, 2, 2, kLoaderTma, kScheduleStreamK},
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 
@@ -980,7 +980,7 @@ bool simt_config_supports(int id, const SimtProblem &p) {
     if (id < 0 || id >= kNumConfigs) return false;
     if (id == 10) return skinny_supports(kSkinnyTall, p);
     if (id == 11) return skinny_supports(kSkinnyWide, p);
-    if (id == 14 || id == 15) return packable(p);
+    if (id == 14 || id == 15 || id == 18) return packable(p);
     if (kConfigs[id].loader == kLoaderTma) return tma_ok(p);
     return true;
 }
@@ -995,7 +995,7 @@ cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const
         case 5: return launch_persistent<128, 256, 2, 4, 4>(kScheduleStreamK, p, stream, detail);
         case 6: return launch_persistent<128, 256, 2, 4, 4>(kSchedulePersistentDP, p, stream, detail);
         case 7: return launch_persistent<256, 128, 4, 2, 4>(kScheduleStreamK, p, stream, detail);
-        case 8: return launch_persistent<128, 128, 2, 2, 3, 248>(kScheduleStreamK, p, stream, detail);
+        case 8: return launch_persistent<128, 128, 2, 2, 3, 255>(kScheduleStreamK, p, stream, detail);
         case 9: return launch_persistent<128, 128, 2, 2, 4, 248>(kScheduleStreamK, p, stream, detail);
         case 10: return skinny_launch(kSkinnyTall, p, stream, detail);
         case 11: return skinny_launch(kSkinnyWide, p, stream, detail);
@@ -1013,6 +1013,7 @@ cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const
         case 17:
             return launch_persistent<256, 128, 4, 2, 2, 255, kLoaderTma, 2>(kScheduleStreamK, p,
                                                                            stream, detail);
+        case 18: return launch_packed(17, p, stream, detail);
         default: *detail = "unknown SIMT configuration"; return cudaErrorInvalidValue;
     }
 }

@@ -173,7 +173,8 @@ def test_each_config(sg, cfg, shape):
 @pytest.mark.parametrize("name", ["sk_tma_ws_128x256_s4", "sk_tma_ws_256x128_s4",
                                   "sk_tma_ws_128x128_s3", "sk_cpasync_128x256_s4",
                                   "sk_cpasync_256x128_s4", "packed_sk_tma_128x256_s4",
-                                  "sk_tma_ws_128x256_k64_s2", "sk_tma_ws_256x128_k64_s2"])
+                                  "sk_tma_ws_128x256_k64_s2", "sk_tma_ws_256x128_k64_s2",
+                                  "packed_sk_tma_256x128_k64_s2"])
 def test_stream_k_deterministic_and_exact(sg, name):
     ids = {sg.sgemm_config_name(i): i for i in range(sg.sgemm_num_configs())}
     sg.sgemm_force_config(ids[name])
@@ -237,7 +238,7 @@ def test_strided_batched(sg, M, N, K, batch, cfg):
         sg.sgemm_force_config(-1)
 
 
-@pytest.mark.parametrize("cfg", [-1, 14, 15])
+@pytest.mark.parametrize("cfg", [-1, 14, 15, 18])
 def test_strided_batched_unaligned(sg, cfg):
     # odd leading dimensions and strides: repacked for TMA (or loaded with cp.async)
     sg.sgemm_force_config(cfg)
