@@ -252,11 +252,20 @@ class OracleTimer:
         return int(min(self.w["M"], max(1, seconds / self.per_row)))
 
 
-def oracle_sample(w, target_s: float, A, B, C):
-    """Times the oracle on a row sample sized for about `target_s` seconds.
-    Returns (gflops, seconds, rows, threads)."""
-    t = OracleTimer(w, A, B, C)
-    dt, n = t.run(t.rows_for(target_s))
+def oracle_sample(w, target_s: float, A, B, C, threads: int | None = None):
+    """Times the oracle on a row sample sized for about `target_s` seconds, on `threads`
+    OpenMP threads (default: all). Returns (gflops, seconds, rows, threads)."""
+    import oracle
+    full = oracle.max_threads()
+    if threads is not None:
+        oracle.set_threads(threads)
+    try:
+        t = OracleTimer(w, A, B, C)
+        if threads is not None:
+            t.threads = threads
+        dt, n = t.run(t.rows_for(target_s))
+    finally:
+        oracle.set_threads(full)
     return 2.0 * n * w["N"] * w["K"] / dt / 1e9, dt, n, t.threads
 
 
@@ -379,16 +388,55 @@ def run_ours(args):
         "e2e": e2e,
         "device": props.name, "sms": sms,
     }
+    if rank == 0 and not args.no_cublas_context:
+        line["context_cublas"] = cublas_context(torch, dev, stream, w, A, B, C, C0, flush,
+                                                max(3, args.warmup), min(args.steps, 50),
+                                                value / world)
     if rank == 0 and not args.no_cpu_baseline:
         gf, dt, nrows, threads = oracle_sample(w, args.cpu_seconds, A_h, B_h, C_h)
         line["cpu_baseline"] = {"value": round(gf, 3), "unit": UNIT, "cores": threads,
                                 "kind": "oracle",
                                 "sample": f"{nrows} of {M} result rows (all N columns, full K), "
                                           f"{dt:.1f} s, fp64 triple loop, OpenMP over rows"}
+        gf1, dt1, n1, _ = oracle_sample(w, args.cpu_seconds / 4, A_h, B_h, C_h, threads=1)
+        line["cpu_baseline"]["single_core"] = {
+            "value": round(gf1, 3), "unit": UNIT, "cores": 1,
+            "sample": f"{n1} of {M} result rows (all N columns, full K), {dt1:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def cublas_context(torch, dev, stream, w, A, B, C, C0, flush, warmup, steps, ours):
+    """The same workload through torch.addmm (cuBLAS SGEMM, TF32 off) under the same timing
+    rules: a comparison bar only, never a path of the library."""
+    M, N, K, alpha, beta = w["M"], w["N"], w["K"], w["alpha"], w["beta"]
+    flops = 2.0 * M * N * K
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    out = torch.empty_like(C)
+    src = C0 if C0 is not None else C
+    try:
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                flush.fill_(1.0)
+                torch.addmm(src, A, B, beta=beta, alpha=alpha, out=out)
+            ms = []
+            for i in range(steps):
+                flush.fill_(float(i))
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                torch.addmm(src, A, B, beta=beta, alpha=alpha, out=out)
+                e1.record(stream)
+                e1.synchronize()
+                ms.append(e0.elapsed_time(e1))
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    gf = flops * len(ms) / (sum(ms) / 1e3) / 1e9
+    return {"value": round(gf, 1), "unit": UNIT, "library": "torch.addmm (cuBLAS SGEMM), TF32 off",
+            "steps": len(ms), "ours_over_it": round(ours / gf, 3)}
 
 
 def run_e2e(args, torch, sg, dev, stream, w, A_h, B_h, C_h, entry, dist, world):
@@ -492,6 +540,8 @@ def parse(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cublas-context", action="store_true",
+                    help="skip timing torch.addmm (cuBLAS) on the same workload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="oracle seconds for the cpu_baseline sample (reference arm: whole run)")
     args = ap.parse_args(argv)

@@ -348,32 +348,33 @@ struct Segment {
 };
 
 // The ordered list of segments (tile, k-range) CTA `c` processes: its data-parallel tiles,
-// then its stream-K range from the last tile backwards.
+// then its stream-K range from the last tile backwards. Only the cursor lives here; the
+// launch constants are read from the kernel parameters at each step, so the cursor costs the
+// hot loop few registers.
 struct SegmentWalker {
-    int t, dp_tiles, G, KT;
-    long long s, cur_end;
+    int t;                  // next data-parallel tile
+    long long s, cur_end;   // stream-K range still to walk: [s, cur_end)
 
-    __device__ SegmentWalker(const PParams &p, int c) {
+    SegmentWalker() = default;
+
+    __device__ void init(const PParams &p, int c) {
         t = c;
-        dp_tiles = p.dp_tiles;
-        G = p.G;
-        KT = p.KT;
         const long long base = static_cast<long long>(p.dp_tiles) * p.KT;
         s = base + c * p.sk_base + min(c, p.sk_rem);
         cur_end = s + p.sk_base + (c < p.sk_rem ? 1 : 0);
     }
 
-    __device__ bool next(Segment &seg) {
-        if (t < dp_tiles) {
+    __device__ bool next(const PParams &p, Segment &seg) {
+        if (t < p.dp_tiles) {
             seg.tile = t;
             seg.k0 = 0;
-            seg.k1 = KT;
-            t += G;
+            seg.k1 = p.KT;
+            t += p.G;
             return true;
         }
         if (cur_end <= s) return false;
-        const long long tile = (cur_end - 1) / KT;
-        const long long tb = tile * KT;
+        const long long tile = (cur_end - 1) / p.KT;
+        const long long tb = tile * p.KT;
         const long long lo = s > tb ? s : tb;
         seg.tile = static_cast<int>(tile);
         seg.k0 = static_cast<int>(lo - tb);
@@ -422,22 +423,29 @@ __device__ __forceinline__ bool wait_flag(const unsigned int *flag, unsigned int
     }
 }
 
-// Streams the k-tiles of a CTA's segment list into the shared-memory ring (thread 0 only).
+// Streams the k-tiles of a CTA's segment list into the shared-memory ring. With the TMA
+// loader it lives in shared memory and only thread 0 touches it, so its state occupies no
+// registers in the compute loop; the cp.async loader keeps one copy per thread.
 struct TmaProducer {
     SegmentWalker walk;
     Segment seg;
     int kt, b, m0, n0;
+    int issued;  // k-tiles issued so far (ring position)
     bool live;
 
-    __device__ TmaProducer(const PParams &p, int c) : walk(p, c), kt(0), b(0), m0(0), n0(0) {
-        live = walk.next(seg);
+    TmaProducer() = default;
+
+    __device__ void init(const PParams &p, int c) {
+        walk.init(p, c);
+        kt = b = m0 = n0 = issued = 0;
+        live = walk.next(p, seg);
         kt = seg.k0;
     }
 
     template <int BM, int BN>
     __device__ bool next(const PParams &p) {
         while (live && kt >= seg.k1) {
-            live = walk.next(seg);
+            live = walk.next(p, seg);
             kt = seg.k0;
         }
         if (!live) return false;
@@ -468,6 +476,7 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
     float *smem = reinterpret_cast<float *>(smem_raw + pad);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_FLOATS);
     __shared__ int s_abort;
+    __shared__ TmaProducer s_prod;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cta = blockIdx.x;
@@ -482,17 +491,18 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
             mbar_init_fence();
         }
     }
-    __syncthreads();
 
     // TMA: thread 0 streams the k-tiles of the CTA's whole segment list into the ring, the
     // first STAGES up front, then one refill into the stage just released after every k-tile.
     // cp.async: every thread walks the same cursor and copies its share of each k-tile; the
     // first STAGES - 1 up front, then, after the barrier that ends k-tile i - 1, k-tile
     // i + STAGES - 1 into the stage k-tile i - 1 used.
-    TmaProducer prod(p, cta);
-    int issued = 0;
+    TmaProducer prod_local;
+    TmaProducer &prod = LOADER == kLoaderTma ? s_prod : prod_local;
+    if (LOADER != kLoaderTma || tid == 0) prod.init(p, cta);
+    __syncthreads();
     auto produce = [&]() {
-        const int s = issued % STAGES;
+        const int s = prod.issued % STAGES;
         float *sA = smem + s * STAGE_FLOATS;
         if (LOADER == kLoaderTma) {
             mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
@@ -508,11 +518,11 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
                 tid);
         }
         ++prod.kt;
-        ++issued;
+        ++prod.issued;
     };
     if (LOADER == kLoaderTma) {
         if (tid == 0)
-            while (issued < STAGES && prod.template next<BM, BN>(p)) produce();
+            while (prod.issued < STAGES && prod.template next<BM, BN>(p)) produce();
     } else {
         for (int s = 0; s < STAGES - 1; ++s) {
             if (prod.template next<BM, BN>(p)) produce();
@@ -522,10 +532,11 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
 
     const int wm0 = (warp / WARPS_N) * 64, wn0 = (warp % WARPS_N) * 64;
     const int tr = lane >> 2, tc = lane & 3;
-    SegmentWalker walk(p, cta);
+    SegmentWalker walk;
+    walk.init(p, cta);
     Segment seg;
     int i = 0;
-    while (walk.next(seg)) {
+    while (walk.next(p, seg)) {
         int b, m0, n0;
         tile_origin(p, seg.tile, BM, BN, b, m0, n0);
         float2 acc[8][8];
@@ -603,7 +614,7 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
     if (LOADER != kLoaderTma) cp_async_wait<0>();
     if (LOADER == kLoaderTma && s_abort && tid == 0) {
         // Let copies already in flight land before the CTA's shared memory is released.
-        for (; i < issued; ++i)
+        for (; i < prod.issued; ++i)
             if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1)) break;
     }
 }

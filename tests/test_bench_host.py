@@ -116,3 +116,13 @@ def test_reference_arm_runs_on_cpu():
     assert line["impl"] == "reference" and line["unit"] == "GFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_oracle_sample_single_core_restores_threads():
+    import oracle
+    full = oracle.max_threads()
+    w = bench.WORKLOADS["sq256"]
+    A, B, C = bench.host_inputs(w)
+    gf, dt, n, threads = bench.oracle_sample(w, 0.05, A, B, C, threads=1)
+    assert threads == 1 and gf > 0 and 1 <= n <= w["M"]
+    assert oracle.max_threads() == full
