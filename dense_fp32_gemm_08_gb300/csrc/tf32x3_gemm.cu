@@ -9,23 +9,29 @@
 // contiguous), so both MMA operands are K-major in shared memory. Non-finite values keep
 // big = x and small = 0, so Inf and NaN propagate as in fp32.
 //
-// GEMM. One CTA per 128 x BN output tile, 6 warps:
+// GEMM. A persistent grid (one CTA per SM) walks the 128 x BN output tiles in grouped-raster
+// order, tile t, t + grid, ...; 6 warps per CTA:
 //   warp 0, lane 0: TMA producer, four boxes per 32-wide k-block (A big/small 128 x 32,
-//                   B big/small BN x 32, 128-byte swizzle) into a STAGES-deep ring;
-//   warp 1:         allocates ACCS x BN TMEM columns; lane 0 issues the MMAs:
-//                   per k-block 4 k-steps x (small_A.big_B, big_A.small_B, big_A.big_B), each
-//                   tcgen05.mma.cta_group::1.kind::tf32 M=128, N=BN, K=8, accumulating in TMEM
-//                   (fp32); k-block kb goes to accumulator kb % ACCS; tcgen05.commit frees the
-//                   stage, a final commit marks the accumulators ready;
+//                   B big/small BN x 32, 128-byte swizzle) into a STAGES-deep ring that runs
+//                   on from one tile into the next;
+//   warp 1:         allocates two sets of ACCS x BN TMEM columns (one per tile in flight);
+//                   lane 0 issues the MMAs: per k-block 4 k-steps x (small_A.big_B,
+//                   big_A.small_B, big_A.big_B), each tcgen05.mma.cta_group::1.kind::tf32
+//                   M=128, N=BN, K=8, accumulating in TMEM (fp32); k-block kb goes to
+//                   accumulator kb % ACCS of the tile's set; tcgen05.commit frees each stage,
+//                   and a commit per tile marks its set ready;
 //   warps 2..5:     epilogue: tcgen05.ld (32 lanes x 32 columns per load) of the TMEM rows the
 //                   warp may access, the ACCS accumulators summed in fp32 in a fixed order,
-//                   alpha * acc + beta * C (C unread when beta == 0), stores.
+//                   alpha * acc + beta * C (C unread when beta == 0), stores; after its last
+//                   load of a tile each warp hands the set back, so tile j's epilogue runs
+//                   while the MMAs of tile j + 1 fill the other set.
 // Why several accumulators: the tensor core's fp32 accumulation loses more than round-to-
 // nearest as the running sum grows (measured: normalised error 7.2e-6 at K = 16384 with one
 // accumulator). The error grows like n^1.5 for n terms per accumulator, so ACCS accumulators
 // over interleaved k-blocks cut it by about sqrt(ACCS).
-// Every wait is bounded; a wait that expires raises the fault word, and the CTA still meets at
-// the final barrier and frees its TMEM.
+// Every wait is bounded; a wait that expires raises the fault word, the role stops, the TMA
+// producer waits (bounded) for the copies it issued to land, and the CTA still meets at the
+// final barrier and frees its TMEM.
 //
 // Single-product mode (PRODUCTS = 1, the "1xTF32" fast path): the pre-pass writes only the big
 // parts (tf32_rna of each value) and the kernel issues big_A.big_B alone, with twice the
@@ -225,10 +231,17 @@ struct TParams {
     long long ldc, sC;
     int batch;
     int tiles_m, tiles_n, group_m;
+    int total_tiles;    // tiles_m * tiles_n * batch
     int c_vec4;
     const float *bias;  // fused epilogue (nullptr: none)
     int act;            // fused epilogue activation (0: none)
 };
+
+__host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
+    uint32_t r = 32;
+    while (r < v) r <<= 1;
+    return r;
+}
 
 template <int BN, int STAGES, int ACCS, int PRODUCTS>
 __global__ void __launch_bounds__(192, 1)
@@ -242,25 +255,26 @@ __global__ void __launch_bounds__(192, 1)
     constexpr uint32_t PARTS = PRODUCTS == 3 ? 2 : 1;  // big (and small) of each operand
     constexpr uint32_t STAGE_BYTES = PARTS * (A_BYTES + B_BYTES);
     constexpr uint32_t IDESC = idesc_tf32(BN);
-    constexpr uint32_t TMEM_COLS = BN * ACCS;
+    constexpr uint32_t SET_COLS = BN * ACCS;                   // one tile's accumulators
+    constexpr uint32_t TMEM_COLS = pow2_at_least(2 * SET_COLS);  // two tiles in flight
+    constexpr uint32_t SET_STRIDE = TMEM_COLS / 2;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
-    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
-                  "TMEM allocations are powers of two from 32 to 512 columns");
+    static_assert(BN % 32 == 0, "the epilogue reads 32-column slices");
+    static_assert(TMEM_COLS <= 512, "two accumulator sets must fit in TMEM");
+    constexpr int EPI_WARPS = 4;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
     uint64_t *empty = full + STAGES;
-    uint64_t *accum_ready = empty + STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum_ready + 1);
+    uint64_t *set_full = empty + STAGES;  // [2]: a tile's accumulators are complete
+    uint64_t *set_free = set_full + 2;    // [2]: the epilogue has read them
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(set_free + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x, b = blockIdx.y;
-    int tm, tn;  // grouped raster: a wave's A and B panels stay in L2
-    tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-    const int m0 = tm * BM, n0 = tn * BN;
     const int KB = (p.K + BK - 1) / BK;
+    const int tiles_per_batch = p.tiles_m * p.tiles_n;
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&mapAhi);
@@ -271,11 +285,13 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accum_ready, 1);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&set_full[j], 1);
+            mbar_init(&set_free[j], EPI_WARPS);
+        }
         mbar_init_fence();
     }
     if (warp == 1) {
-        // TMEM: ACCS accumulators of BN columns x 128 lanes of fp32.
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(tmem_slot)),
                      "r"(TMEM_COLS)
@@ -287,103 +303,143 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Output tile t of the persistent walk: batch entry b, origin (m0, n0).
+    auto tile_origin = [&](int t, int &b, int &m0, int &n0) {
+        b = t / tiles_per_batch;
+        int tm, tn;  // grouped raster: concurrently running tiles share A and B panels in L2
+        tile_coords(t - b * tiles_per_batch, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        m0 = tm * BM;
+        n0 = tn * BN;
+    };
+
     if (warp == 0 && lane == 0) {
         // ---- TMA producer ----
-        for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % STAGES;
-            if (kb >= STAGES && !mbar_wait(&empty[s], ((kb / STAGES) - 1) & 1)) break;
-            uint8_t *st = smem + s * STAGE_BYTES;
-            mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-            tma_load_3d(st, &mapAhi, &full[s], kb * BK, m0, b);
-            tma_load_3d(st + PARTS * A_BYTES, &mapBhi, &full[s], kb * BK, n0, b);
-            if (PRODUCTS == 3) {
-                tma_load_3d(st + A_BYTES, &mapAlo, &full[s], kb * BK, m0, b);
-                tma_load_3d(st + 2 * A_BYTES + B_BYTES, &mapBlo, &full[s], kb * BK, n0, b);
-            }
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer ----
+        int it = 0;  // ring position over every k-block of every tile
         bool ok = true;
-        for (int kb = 0; kb < KB && ok; ++kb) {
-            const int s = kb % STAGES;
-            if (!mbar_wait(&full[s], (kb / STAGES) & 1)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t st = smem_addr(smem + s * STAGE_BYTES);
-            const uint32_t a_hi = st, a_lo = st + A_BYTES;
-            const uint32_t b_hi = st + PARTS * A_BYTES, b_lo = b_hi + B_BYTES;
-            const uint32_t d = tmem + static_cast<uint32_t>((kb % ACCS) * BN);
-#pragma unroll
-            for (int kk = 0; kk < BK / 8; ++kk) {
-                const uint32_t off = kk * 32;  // 8 tf32 values along k
-                const uint32_t acc0 = (kb >= ACCS || kk > 0) ? 1u : 0u;  // first write: overwrite
+        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            int b, m0, n0;
+            tile_origin(t, b, m0, n0);
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int s = it % STAGES;
+                if (it >= STAGES && !mbar_wait(&empty[s], ((it / STAGES) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = smem + s * STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                tma_load_3d(st, &mapAhi, &full[s], kb * BK, m0, b);
+                tma_load_3d(st + PARTS * A_BYTES, &mapBhi, &full[s], kb * BK, n0, b);
                 if (PRODUCTS == 3) {
-                    mma_tf32(d, smem_desc_sw128(a_lo + off), smem_desc_sw128(b_hi + off), IDESC, acc0);
-                    mma_tf32(d, smem_desc_sw128(a_hi + off), smem_desc_sw128(b_lo + off), IDESC, 1u);
-                    mma_tf32(d, smem_desc_sw128(a_hi + off), smem_desc_sw128(b_hi + off), IDESC, 1u);
-                } else {
-                    mma_tf32(d, smem_desc_sw128(a_hi + off), smem_desc_sw128(b_hi + off), IDESC, acc0);
+                    tma_load_3d(st + A_BYTES, &mapAlo, &full[s], kb * BK, m0, b);
+                    tma_load_3d(st + 2 * A_BYTES + B_BYTES, &mapBlo, &full[s], kb * BK, n0, b);
                 }
             }
-            mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
-        mma_commit(accum_ready);  // arrives when every MMA issued above has completed
+        // The CTA's shared memory must outlive every copy: wait (bounded) for the last
+        // STAGES issued to land; stages the MMAs already consumed complete at once.
+        for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
+            if (!mbar_wait(&full[j % STAGES], (j / STAGES) & 1)) break;
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer ----
+        int it = 0, j = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++j) {
+            const int set = j & 1;
+            if (j >= 2 && !mbar_wait(&set_free[set], ((j >> 1) - 1) & 1)) break;
+            tc_fence_after();
+            const uint32_t dset = tmem + static_cast<uint32_t>(set) * SET_STRIDE;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int s = it % STAGES;
+                if (!mbar_wait(&full[s], (it / STAGES) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t st = smem_addr(smem + s * STAGE_BYTES);
+                const uint32_t a_hi = st, a_lo = st + A_BYTES;
+                const uint32_t b_hi = st + PARTS * A_BYTES, b_lo = b_hi + B_BYTES;
+                const uint32_t d = dset + static_cast<uint32_t>((kb % ACCS) * BN);
+#pragma unroll
+                for (int kk = 0; kk < BK / 8; ++kk) {
+                    const uint32_t off = kk * 32;  // 8 tf32 values along k
+                    const uint32_t acc0 = (kb >= ACCS || kk > 0) ? 1u : 0u;  // first: overwrite
+                    if (PRODUCTS == 3) {
+                        mma_tf32(d, smem_desc_sw128(a_lo + off), smem_desc_sw128(b_hi + off), IDESC, acc0);
+                        mma_tf32(d, smem_desc_sw128(a_hi + off), smem_desc_sw128(b_lo + off), IDESC, 1u);
+                        mma_tf32(d, smem_desc_sw128(a_hi + off), smem_desc_sw128(b_hi + off), IDESC, 1u);
+                    } else {
+                        mma_tf32(d, smem_desc_sw128(a_hi + off), smem_desc_sw128(b_hi + off), IDESC, acc0);
+                    }
+                }
+                mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+            }
+            if (ok) mma_commit(&set_full[set]);  // arrives when this tile's MMAs are complete
+        }
     } else if (warp >= 2) {
         // ---- epilogue: TMEM -> registers -> C ----
         const int quarter = warp & 3;  // TMEM lanes this warp may access
-        const bool ready = mbar_wait(accum_ready, 0);
-        tc_fence_after();
-        if (ready && KB > 0) {
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const int used = KB < ACCS ? KB : ACCS;  // accumulators that received k-blocks
+        const float alpha = p.alpha, beta = p.beta;
+        int j = 0;
+        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++j) {
+            const int set = j & 1;
+            if (!mbar_wait(&set_full[set], (j >> 1) & 1)) break;
+            tc_fence_after();
+            int b, m0, n0;
+            tile_origin(t, b, m0, n0);
+            const uint32_t tset = tmem + lane_base + static_cast<uint32_t>(set) * SET_STRIDE;
             const int row = m0 + quarter * 32 + lane;
             float *crow = p.C + static_cast<long long>(b) * p.sC + static_cast<long long>(row) * p.ldc;
-            const float alpha = p.alpha, beta = p.beta;
 #pragma unroll 1
-            const int used = KB < ACCS ? KB : ACCS;  // accumulators that received k-blocks
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float v[32];
-                const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-                tmem_ld_32x32b_x32(tmem + lane_base + c0, v);
-                for (int j = 1; j < used; ++j) {
+                tmem_ld_32x32b_x32(tset + c0, v);
+                for (int a = 1; a < used; ++a) {
                     float w[32];
-                    tmem_ld_32x32b_x32(tmem + lane_base + static_cast<uint32_t>(j * BN + c0), w);
+                    tmem_ld_32x32b_x32(tset + static_cast<uint32_t>(a * BN + c0), w);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] += w[i];
                 }
-                if (row >= p.M) continue;
+                if (c0 + 32 >= BN) {
+                    // Last slice read: hand the set back to the MMA issuer.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&set_free[set]);
+                }
+                if (row >= p.M || KB == 0) continue;
                 const int col0 = n0 + c0;
                 if (p.bias != nullptr || p.act != kActNone) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = col0 + j;
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int col = col0 + jj;
                         if (col < p.N)
-                            crow[col] = epilogue_value(v[j], alpha, beta, p.bias, col, p.act,
+                            crow[col] = epilogue_value(v[jj], alpha, beta, p.bias, col, p.act,
                                                        crow + col);
                     }
                 } else if (p.c_vec4 && col0 + 31 < p.N) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
+                    for (int jj = 0; jj < 32; jj += 4) {
                         float4 o;
                         if (beta != 0.0f) {
-                            const float4 c = *reinterpret_cast<const float4 *>(crow + col0 + j);
-                            o = make_float4(fmaf(alpha, v[j], beta * c.x),
-                                            fmaf(alpha, v[j + 1], beta * c.y),
-                                            fmaf(alpha, v[j + 2], beta * c.z),
-                                            fmaf(alpha, v[j + 3], beta * c.w));
+                            const float4 c = *reinterpret_cast<const float4 *>(crow + col0 + jj);
+                            o = make_float4(fmaf(alpha, v[jj], beta * c.x),
+                                            fmaf(alpha, v[jj + 1], beta * c.y),
+                                            fmaf(alpha, v[jj + 2], beta * c.z),
+                                            fmaf(alpha, v[jj + 3], beta * c.w));
                         } else {
-                            o = make_float4(alpha * v[j], alpha * v[j + 1], alpha * v[j + 2],
-                                            alpha * v[j + 3]);
+                            o = make_float4(alpha * v[jj], alpha * v[jj + 1], alpha * v[jj + 2],
+                                            alpha * v[jj + 3]);
                         }
-                        *reinterpret_cast<float4 *>(crow + col0 + j) = o;
+                        *reinterpret_cast<float4 *>(crow + col0 + jj) = o;
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = col0 + j;
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int col = col0 + jj;
                         if (col < p.N)
-                            crow[col] = beta != 0.0f ? fmaf(alpha, v[j], beta * crow[col])
-                                                     : alpha * v[j];
+                            crow[col] = beta != 0.0f ? fmaf(alpha, v[jj], beta * crow[col])
+                                                     : alpha * v[jj];
                     }
                 }
             }
@@ -391,7 +447,7 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     tc_fence_before();
-    __syncthreads();  // every role is done with the ring and the accumulator
+    __syncthreads();  // every role is done with the ring and the accumulators
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -477,11 +533,22 @@ bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u
 
 constexpr int kMaxDevices = 64;
 
+// Multiprocessors of device `dev` (queried once), or 0 if the query fails.
+int sm_count(int dev) {
+    static std::once_flag once[kMaxDevices];
+    static int count[kMaxDevices];
+    std::call_once(once[dev], [&] {
+        if (cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            count[dev] = 0;
+    });
+    return count[dev];
+}
+
 template <int BN, int STAGES, int ACCS, int PRODUCTS>
 cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char **detail) {
     constexpr size_t PARTS = PRODUCTS == 3 ? 2 : 1;
     constexpr size_t STAGE_BYTES = PARTS * (BM * BK * 4 + static_cast<size_t>(BN) * BK * 4);
-    constexpr size_t SMEM = STAGES * STAGE_BYTES + (2 * STAGES + 1) * 8 + 16 + 1024;
+    constexpr size_t SMEM = STAGES * STAGE_BYTES + (2 * STAGES + 4) * 8 + 16 + 1024;
     auto kernel = tf32x3_gemm_kernel<BN, STAGES, ACCS, PRODUCTS>;
 
     int dev = 0;
@@ -499,6 +566,11 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
     if (attr_err[dev] != cudaSuccess) {
         *detail = "cudaFuncSetAttribute(max dynamic shared memory) failed";
         return attr_err[dev];
+    }
+    const int sms = sm_count(dev);
+    if (sms <= 0) {
+        *detail = "multiprocessor count query failed";
+        return cudaErrorInvalidDevice;
     }
 
     // Split workspace: A parts M x ldk, B parts N x ldk (ldk = K rounded up to 4 so rows
@@ -599,49 +671,72 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
     tp.c_vec4 = aligned16(p.C) && p.ldc % 4 == 0 && (p.batch <= 1 || p.strideC % 4 == 0);
     tp.bias = p.bias;
     tp.act = p.act;
-    const long long tiles = static_cast<long long>(tp.tiles_m) * tp.tiles_n;
-    if (tiles > 0x7fffffffLL || p.batch > 65535) {
-        *detail = "too many output tiles or batch entries for the 3xTF32 grid";
+    const long long tiles = static_cast<long long>(tp.tiles_m) * tp.tiles_n * p.batch;
+    if (tiles > 0x7fffffffLL) {
+        *detail = "too many output tiles for the tensor-core grid";
         return cudaErrorInvalidValue;
     }
-    kernel<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(p.batch)), 192, SMEM,
-             stream>>>(mAhi, mAlo, mBhi, mBlo, tp);
+    tp.total_tiles = static_cast<int>(tiles);
+    const int grid = static_cast<int>(std::min<long long>(tiles, sms));  // one CTA per SM
+    kernel<<<grid, 192, SMEM, stream>>>(mAhi, mAlo, mBhi, mBlo, tp);
     err = cudaGetLastError();
     if (err != cudaSuccess) *detail = "3xTF32 kernel launch failed";
     return err;
 }
 
-// Tile width of the tensor paths. Measured on a GB300 (TFLOP/s, fp32-equivalent):
-//   1xTF32  4096^3: N=128 421, N=256 535;  16384x12288x4096: N=128 461, N=256 654
-//   3xTF32  4096^3: N=128 241, N=256 217;  16384x12288x4096: N=128 266, N=256 270
-// N = 256 halves the A operand's shared-memory reads per unit of MMA work, which is what
-// bounds these kernels; 3xTF32 at N = 256 has only two stages and fewer, larger tiles, so it
-// wins only once the grid is several waves deep. SGEMM_TF32_TILE_N=128|256 forces a width.
-int tensor_tile_n(const SimtProblem &p, bool three_products) {
+// Tile width of the tensor paths. The persistent grid runs ceil(tiles / SMs) rounds of tiles;
+// a round costs the MMA time of one tile, proportional to BN, divided by the width's
+// efficiency (narrower tiles read more shared memory per MMA; measured on a GB300 at
+// 16384 x 14336 x 4096: 192 columns run at 0.953 of the rate of 256, 224 interpolated at
+// 0.975). The single-product path takes the width in {256, 224, 192} with the lowest
+// rounds x BN / efficiency (4096 x 4096: 608 tiles of 224 = 4 rounds, 627 TFLOP/s, against
+// 548 for 4 rounds of 256 and 550 for 5 rounds of 192; 16384 x 14336: 256). The 3xTF32
+// path keeps BN = 128: its two accumulators per tile (for accuracy) times two tiles in
+// flight fill the 512 TMEM columns. SGEMM_TF32_TILE_N=192|224|256 forces the width.
+int tf32_tile_n(const SimtProblem &p, int sms) {
     static const int forced = [] {
         const char *env = std::getenv("SGEMM_TF32_TILE_N");
-        if (env && std::strcmp(env, "256") == 0) return 256;
-        if (env && std::strcmp(env, "128") == 0) return 128;
-        return 0;
+        if (!env) return 0;
+        const int v = std::atoi(env);
+        return v == 192 || v == 224 || v == 256 ? v : 0;
     }();
     if (forced) return forced;
-    if (!three_products) return 256;
-    const long long tiles256 = static_cast<long long>((p.M + BM - 1) / BM) * ((p.N + 255) / 256) * p.batch;
-    return tiles256 >= 6LL * 152 ? 256 : 128;
+    const long long tm = (p.M + BM - 1) / BM;
+    constexpr int widths[3] = {256, 224, 192};
+    constexpr int efficiency_milli[3] = {1000, 975, 953};
+    int best = 256;
+    long long best_cost = -1;
+    for (int w = 0; w < 3; ++w) {
+        const int bn = widths[w];
+        const long long tiles = tm * ((p.N + bn - 1) / bn) * p.batch;
+        const long long cost = (tiles + sms - 1) / sms * bn * 1000 / efficiency_milli[w];
+        if (best_cost < 0 || cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 }  // namespace
 
-bool tf32x3_supports(const SimtProblem &p) { return p.batch <= 65535; }
+bool tf32x3_supports(const SimtProblem &p) { return p.batch >= 1; }
 
 cudaError_t tf32x3_launch(const SimtProblem &p, cudaStream_t stream, const char **detail) {
-    if (tensor_tile_n(p, true) == 256) return launch_tf32x3<256, 2, 2, 3>(p, stream, detail);
-    return launch_tf32x3<128, 3, 4, 3>(p, stream, detail);
+    return launch_tf32x3<128, 3, 2, 3>(p, stream, detail);
 }
 
 cudaError_t tf32_launch(const SimtProblem &p, cudaStream_t stream, const char **detail) {
-    if (tensor_tile_n(p, false) == 256) return launch_tf32x3<256, 4, 2, 1>(p, stream, detail);
-    return launch_tf32x3<128, 6, 4, 1>(p, stream, detail);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *detail = "cudaGetDevice failed";
+        return cudaErrorInvalidDevice;
+    }
+    switch (tf32_tile_n(p, std::max(1, sm_count(dev)))) {
+        case 192: return launch_tf32x3<192, 5, 1, 1>(p, stream, detail);
+        case 224: return launch_tf32x3<224, 5, 1, 1>(p, stream, detail);
+        default: return launch_tf32x3<256, 4, 1, 1>(p, stream, detail);
+    }
 }
 
 cudaError_t tf32x3_release_workspaces() {

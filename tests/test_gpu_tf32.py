@@ -81,3 +81,13 @@ def test_strided_batched(sgemm_lib):
         den = oracle.absdot(M, N, K, a, K, bb, N)
         got = out[b * sC:b * sC + M * N].reshape(M, N)
         assert oracle.normalized_error(got, ref, den, 0.7, -1.3, c.reshape(M, N)) <= TOL_TF32
+
+
+# The persistent kernel picks its tile width (192, 224 or 256 columns) from the number of
+# rounds of tiles the grid needs; each shape below selects one width and gives every CTA
+# at least three tiles, so both TMEM accumulator sets are reused.
+@pytest.mark.parametrize("M,N,width", [(1280, 7744, 192), (1408, 7936, 224), (1664, 7872, 256)])
+def test_each_tile_width(sgemm_lib, M, N, width):
+    got, ref, _ = _check(Case(M, N, 64, 1.0, -1.0, "small_int", seed=11), sgemm_lib)
+    assert np.array_equal(got, ref)
+    _check(Case(M, N, 200, 0.7, 0.5, "normal", seed=12, rows=sample_rows(M)), sgemm_lib)
