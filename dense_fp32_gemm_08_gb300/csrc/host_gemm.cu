@@ -1,14 +1,18 @@
 // host_gemm.cu: C = alpha * (A . B) + beta * C with A, B and C in host memory.
 //
-// B is uploaded once; the rows of A (and of C when beta != 0) then travel in chunks through
-// two device buffers each, on an upload stream, while the caller's stream computes the
-// previous chunk and a download stream returns the chunk before that. With page-locked host
-// memory the copies overlap the GEMMs, so a long product runs at the slower of the copy rate
-// and the kernel rate instead of their sum; with pageable memory everything runs in order on
-// the caller's stream. Every chunk is computed by the same device
-// entry point (the SIMT path, with its per-shape configuration).
+// The rows of A (and of C when beta != 0) travel in chunks through two device buffers each,
+// on an upload stream, while the caller's stream computes the previous chunk and a download
+// stream returns the chunk before that. With page-locked host memory the copies overlap the
+// GEMMs, so a long product runs at the slower of the copy rate and the kernel rate instead
+// of their sum; with pageable memory everything runs in order on the caller's stream.
+// B must be on the device before the first chunk can finish, so the first chunk is computed
+// as K slices, each starting as soon as its rows of B and columns of A have arrived (later
+// slices accumulate into C with beta = 1): the GPU starts after a quarter of B instead of
+// all of it. Every GEMM is computed by the same device entry point (the SIMT path, with its
+// per-shape configuration).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -20,7 +24,7 @@ namespace {
 struct HostPath {
     int dev = -1;
     cudaStream_t up = nullptr, down = nullptr;
-    cudaEvent_t b_ready = nullptr;
+    cudaEvent_t caller_done = nullptr;
     cudaEvent_t in_ready[2] = {nullptr, nullptr};
     cudaEvent_t computed[2] = {nullptr, nullptr};
     cudaEvent_t out_done[2] = {nullptr, nullptr};
@@ -43,7 +47,7 @@ cudaError_t host_path(int dev, HostPath **out) {
     h->dev = dev;
     cudaError_t err = cudaStreamCreateWithFlags(&h->up, cudaStreamNonBlocking);
     if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&h->down, cudaStreamNonBlocking);
-    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&h->b_ready, cudaEventDisableTiming);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&h->caller_done, cudaEventDisableTiming);
     for (int i = 0; i < 2 && err == cudaSuccess; ++i) {
         err = cudaEventCreateWithFlags(&h->in_ready[i], cudaEventDisableTiming);
         if (err == cudaSuccess) err = cudaEventCreateWithFlags(&h->computed[i], cudaEventDisableTiming);
@@ -69,6 +73,14 @@ bool page_locked(const void *ptr) {
     return attr.type == cudaMemoryTypeHost;
 }
 
+// Copies `rows` rows of `width` bytes; one linear copy when both sides are contiguous.
+cudaError_t copy_rows(void *dst, size_t dpitch, const void *src, size_t spitch, size_t width,
+                      size_t rows, cudaMemcpyKind kind, cudaStream_t stream) {
+    if (dpitch == width && spitch == width)
+        return cudaMemcpyAsync(dst, src, width * rows, kind, stream);
+    return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, stream);
+}
+
 }  // namespace
 
 cudaError_t host_gemm(const HostProblem &p, cudaStream_t stream, DeviceGemmFn gemm,
@@ -87,15 +99,24 @@ cudaError_t host_gemm(const HostProblem &p, cudaStream_t stream, DeviceGemmFn ge
     }
     std::lock_guard<std::mutex> lock(h->mu);
 
-    // Chunks of about an eighth of M, whole 128-row tiles, at least 128 rows.
+    // Chunks of whole 128-row tiles, at least an eighth of M, grown until one chunk holds a
+    // full wave of 128 x 256 tiles (so each chunk GEMM fills the GPU), at most M.
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 1;
     long long mc = (p.M + 7) / 8;
     mc = (mc + 127) / 128 * 128;
     if (mc < 128) mc = 128;
+    const long long tiles_n = (p.N + 255) / 256;
+    while (mc < p.M && (mc / 128) * tiles_n < sms) mc *= 2;
     if (mc > p.M) mc = p.M;
-    const long long ldk = p.K, ldn = p.N;  // packed device copies
-    const size_t b_elems = static_cast<size_t>(p.K) * ldn;
-    const size_t a_elems = static_cast<size_t>(mc) * ldk;
-    const size_t c_elems = static_cast<size_t>(mc) * ldn;
+    // Device copies with rows padded to 16 bytes and buffers 256-byte aligned, so the
+    // chunk GEMMs can always read them with TMA.
+    const long long ldk = (p.K + 3) / 4 * 4, ldn = (p.N + 3) / 4 * 4;
+    auto round64 = [](size_t n) { return (n + 63) / 64 * 64; };
+    const size_t b_elems = round64(static_cast<size_t>(p.K) * ldn);
+    const size_t a_elems = round64(static_cast<size_t>(mc) * ldk);
+    const size_t c_elems = round64(static_cast<size_t>(mc) * ldn);
     const size_t need = (b_elems + 2 * a_elems + 2 * c_elems) * sizeof(float);
     if (h->bytes < need) {
         if (h->buf) {
@@ -126,47 +147,78 @@ cudaError_t host_gemm(const HostProblem &p, cudaStream_t stream, DeviceGemmFn ge
     cudaStream_t up = overlap ? h->up : stream;
     cudaStream_t down = overlap ? h->down : stream;
 
+    // The first chunk in K slices of at least 256 (multiples of 32), at most four.
+    const int kslices = reads_ab ? static_cast<int>(std::min<long long>(4, p.K / 256)) : 1;
+    const long long kc = kslices > 1 ? ((p.K + kslices - 1) / kslices + 31) / 32 * 32 : p.K;
+
     // The upload stream starts after everything already queued on the caller's stream.
-    err = cudaEventRecord(h->b_ready, stream);
-    if (err == cudaSuccess) err = cudaStreamWaitEvent(up, h->b_ready, 0);
-    if (err == cudaSuccess && reads_ab)
-        err = cudaMemcpy2DAsync(dB, ldn * sizeof(float), p.B, p.ldb * sizeof(float),
-                                p.N * sizeof(float), p.K, cudaMemcpyHostToDevice, up);
-    if (err == cudaSuccess) err = cudaEventRecord(h->b_ready, up);
+    err = cudaEventRecord(h->caller_done, stream);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(up, h->caller_done, 0);
     if (err != cudaSuccess) {
-        *detail = "uploading B failed";
+        *detail = "ordering the upload stream failed";
         return err;
     }
 
-    const long long chunks = (p.M + mc - 1) / mc;
+    // Row chunks of mc rows; the last one (when it has at least 256 rows) in two halves, so
+    // the download that ends the call is half as long.
+    std::vector<long long> starts;
+    for (long long r = 0; r < p.M; r += mc) starts.push_back(r);
+    const long long last = starts.back(), last_rows = p.M - last;
+    if (starts.size() > 1 && last_rows >= 256) starts.push_back(last + (last_rows / 2 + 127) / 128 * 128);
+    starts.push_back(p.M);
+    const long long chunks = static_cast<long long>(starts.size()) - 1;
     for (long long i = 0; i < chunks; ++i) {
         const int j = static_cast<int>(i & 1);
-        const long long r0 = i * mc;
-        const long long rows = (p.M - r0) < mc ? (p.M - r0) : mc;
+        const long long r0 = starts[i];
+        const long long rows = starts[i + 1] - r0;
         // buffer j is free once chunk i - 2 has been downloaded
         if (i >= 2) err = cudaStreamWaitEvent(up, h->out_done[j], 0);
-        if (err == cudaSuccess && reads_ab)
-            err = cudaMemcpy2DAsync(dA[j], ldk * sizeof(float), p.A + r0 * p.lda,
-                                    p.lda * sizeof(float), p.K * sizeof(float), rows,
-                                    cudaMemcpyHostToDevice, up);
         if (err == cudaSuccess && reads_c)
-            err = cudaMemcpy2DAsync(dC[j], ldn * sizeof(float), p.C + r0 * p.ldc,
+            err = copy_rows(dC[j], ldn * sizeof(float), p.C + r0 * p.ldc,
                                     p.ldc * sizeof(float), p.N * sizeof(float), rows,
                                     cudaMemcpyHostToDevice, up);
-        if (err == cudaSuccess) err = cudaEventRecord(h->in_ready[j], up);
-        if (err == cudaSuccess) err = cudaStreamWaitEvent(stream, h->in_ready[j], 0);
-        if (err == cudaSuccess) err = cudaStreamWaitEvent(stream, h->b_ready, 0);
-        if (err != cudaSuccess) {
-            *detail = "queuing a chunk's upload failed";
-            return err;
+        if (i == 0 && kslices > 1) {
+            for (long long k0 = 0; k0 < p.K && err == cudaSuccess; k0 += kc) {
+                const long long kn = (p.K - k0) < kc ? (p.K - k0) : kc;
+                err = copy_rows(dB + k0 * ldn, ldn * sizeof(float), p.B + k0 * p.ldb,
+                                        p.ldb * sizeof(float), p.N * sizeof(float), kn,
+                                        cudaMemcpyHostToDevice, up);
+                if (err == cudaSuccess)
+                    err = copy_rows(dA[0] + k0, ldk * sizeof(float), p.A + k0,
+                                            p.lda * sizeof(float), kn * sizeof(float), rows,
+                                            cudaMemcpyHostToDevice, up);
+                if (err == cudaSuccess) err = cudaEventRecord(h->in_ready[0], up);
+                if (err == cudaSuccess) err = cudaStreamWaitEvent(stream, h->in_ready[0], 0);
+                if (err != cudaSuccess) {
+                    *detail = "queuing a K slice's upload failed";
+                    return err;
+                }
+                err = gemm(rows, p.N, kn, p.alpha, dA[0] + k0, ldk, dB + k0 * ldn, ldn,
+                           k0 == 0 ? p.beta : 1.0f, dC[0], ldn, stream, detail);
+                if (err != cudaSuccess) return err;
+            }
+        } else {
+            if (i == 0 && err == cudaSuccess && reads_ab)
+                err = copy_rows(dB, ldn * sizeof(float), p.B, p.ldb * sizeof(float),
+                                        p.N * sizeof(float), p.K, cudaMemcpyHostToDevice, up);
+            if (err == cudaSuccess && reads_ab)
+                err = copy_rows(dA[j], ldk * sizeof(float), p.A + r0 * p.lda,
+                                        p.lda * sizeof(float), p.K * sizeof(float), rows,
+                                        cudaMemcpyHostToDevice, up);
+            if (err == cudaSuccess) err = cudaEventRecord(h->in_ready[j], up);
+            if (err == cudaSuccess) err = cudaStreamWaitEvent(stream, h->in_ready[j], 0);
+            if (err != cudaSuccess) {
+                *detail = "queuing a chunk's upload failed";
+                return err;
+            }
+            err = gemm(rows, p.N, p.K, p.alpha, dA[j], ldk, dB, ldn, p.beta, dC[j], ldn, stream,
+                       detail);
+            if (err != cudaSuccess) return err;
         }
-        err = gemm(rows, p.N, p.K, p.alpha, dA[j], ldk, dB, ldn, p.beta, dC[j], ldn, stream,
-                   detail);
-        if (err != cudaSuccess) return err;
         err = cudaEventRecord(h->computed[j], stream);
         if (err == cudaSuccess) err = cudaStreamWaitEvent(down, h->computed[j], 0);
         if (err == cudaSuccess)
-            err = cudaMemcpy2DAsync(p.C + r0 * p.ldc, p.ldc * sizeof(float), dC[j],
+            err = copy_rows(p.C + r0 * p.ldc, p.ldc * sizeof(float), dC[j],
                                     ldn * sizeof(float), p.N * sizeof(float), rows,
                                     cudaMemcpyDeviceToHost, down);
         if (err == cudaSuccess) err = cudaEventRecord(h->out_done[j], down);
