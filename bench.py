@@ -383,7 +383,7 @@ def run_ours(args):
         "roofline": roof,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "clock_samples": clk["samples"],
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_call(args.path, kernel, w),
         "wall_s_timed_loop": round(wall, 4),
         "e2e": e2e,
         "device": props.name, "sms": sms,
@@ -406,6 +406,19 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def launches_per_call(path: str, kernel: str, w) -> int:
+    """Kernels one library call launches for the bench's operands (lda = K, ldb = N,
+    ldc = N, 16-byte-aligned allocations): the tensor paths split A, split-and-transpose B,
+    then run the GEMM; a repacked SIMT configuration first copies each operand whose rows
+    TMA cannot read (K or N not a multiple of 4) into aligned storage."""
+    if path in ("3xtf32", "tf32"):
+        return 3
+    n = 1
+    if kernel.startswith("packed"):
+        n += int(w["K"] % 4 != 0) + int(w["N"] % 4 != 0)
+    return n
 
 
 def cublas_context(torch, dev, stream, w, A, B, C, C0, flush, warmup, steps, ours):

@@ -126,3 +126,10 @@ def test_oracle_sample_single_core_restores_threads():
     gf, dt, n, threads = bench.oracle_sample(w, 0.05, A, B, C, threads=1)
     assert threads == 1 and gf > 0 and 1 <= n <= w["M"]
     assert oracle.max_threads() == full
+
+
+def test_launches_per_call():
+    w = {"M": 4095, "N": 3001, "K": 1537}
+    assert bench.launches_per_call("simt", "sk_tma_ws_128x256_k64_s2", bench.WORKLOADS["headline"]) == 1
+    assert bench.launches_per_call("simt", "packed_sk_tma_128x256_s4", w) == 3
+    assert bench.launches_per_call("3xtf32", "tf32x3_tcgen05", w) == 3
