@@ -57,10 +57,25 @@ struct KParams {
     int act;            // fused epilogue activation (0: none)
 };
 
+// Orders in which one k-step's 64 paired FMAs of a thread tile are issued. Every accumulator
+// still sums its k-steps in ascending order, so all orders give identical results; they
+// differ in how ptxas interleaves the FMAs with the next fragment loads. Measured on a GB300
+// at 4096^3 (TFLOP/s, row-outer order / these orders): data-parallel 128x128 62.3 / 63.8 with
+// kOrderHalfSnake, stream-K 128x256 with 32-wide stages 62.4 / 63.0 with kOrderHalfSnake,
+// stream-K 128x256 with 64-wide stages 63.9 / 65.2 with kOrderColumnSnake (64.7 with
+// kOrderHalfSnake); 8192^3 data-parallel 128x128 65.7 / 67.5. The persistent kernels with the
+// cp.async loader take kOrderColumnSnake too: with kOrderHalfSnake they spill registers.
+enum InnerOrder : int {
+    // column chunk q outer, rows inner, the row order reversed on every other chunk
+    kOrderColumnSnake = 0,
+    // column chunk q, then its two column pairs, then rows, reversed on every other pair
+    kOrderHalfSnake = 1,
+};
+
 // One k-tile (32 k-steps) of outer products for one thread's 8 x 16 tile.
 //   a_base: sA + (wm0 + tr) * 32, row r of the thread tile is 8 * r rows further (256 floats).
 //   b_base: sB + wn0 + 4 * tc, chunk q of the thread tile is 16 * q floats further.
-template <int BN>
+template <int BN, int ORDER>
 __device__ __forceinline__ void compute_ktile(const float *__restrict__ a_base, int tr,
                                               const float *__restrict__ b_base,
                                               float2 (&acc)[8][8]) {
@@ -77,15 +92,32 @@ __device__ __forceinline__ void compute_ktile(const float *__restrict__ a_base, 
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 b[q] = *reinterpret_cast<const float4 *>(b_base + (kg * 4 + kk) * BN + 16 * q);
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
+            auto a_pair = [&](int r) {
                 const float av = kk == 0 ? a[r].x : kk == 1 ? a[r].y : kk == 2 ? a[r].z : a[r].w;
-                const float2 a2 = make_float2(av, av);
+                return make_float2(av, av);
+            };
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    acc[r][2 * q] = __ffma2_rn(a2, make_float2(b[q].x, b[q].y), acc[r][2 * q]);
-                    acc[r][2 * q + 1] =
-                        __ffma2_rn(a2, make_float2(b[q].z, b[q].w), acc[r][2 * q + 1]);
+            for (int q = 0; q < 4; ++q) {
+                if (ORDER == kOrderColumnSnake) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = (q & 1) ? 7 - i : i;
+                        const float2 a2 = a_pair(r);
+                        acc[r][2 * q] = __ffma2_rn(a2, make_float2(b[q].x, b[q].y), acc[r][2 * q]);
+                        acc[r][2 * q + 1] =
+                            __ffma2_rn(a2, make_float2(b[q].z, b[q].w), acc[r][2 * q + 1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float2 bp = h == 0 ? make_float2(b[q].x, b[q].y)
+                                                 : make_float2(b[q].z, b[q].w);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int r = h ? 7 - i : i;
+                            acc[r][2 * q + h] = __ffma2_rn(a_pair(r), bp, acc[r][2 * q + h]);
+                        }
+                    }
                 }
             }
         }
@@ -261,7 +293,8 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, 1)
                 const int s = consumed % STAGES;
                 if (!mbar_wait(&full[s], (consumed / STAGES) & 1)) s_abort = 1;
                 const float *sA = smem + s * STAGE_FLOATS;
-                compute_ktile<BN>(sA + (wm0 + tr) * BK, tr, sA + A_FLOATS + wn0 + 4 * tc, acc);
+                compute_ktile<BN, kOrderHalfSnake>(sA + (wm0 + tr) * BK, tr,
+                                                   sA + A_FLOATS + wn0 + 4 * tc, acc);
                 ++consumed;
                 __syncthreads();  // every warp is done reading stage s
                 if (s_abort) break;
@@ -295,7 +328,8 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, 1)
                 }
                 cp_async_commit();
                 const float *sA = smem + (kt % STAGES) * STAGE_FLOATS;
-                compute_ktile<BN>(sA + (wm0 + tr) * BK, tr, sA + A_FLOATS + wn0 + 4 * tc, acc);
+                compute_ktile<BN, kOrderHalfSnake>(sA + (wm0 + tr) * BK, tr,
+                                                   sA + A_FLOATS + wn0 + 4 * tc, acc);
             }
             cp_async_wait<0>();
             __syncthreads();
@@ -558,8 +592,10 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
             const float *sA = smem + s * STAGE_FLOATS;
 #pragma unroll
             for (int j = 0; j < KSUB; ++j)
-                compute_ktile<BN>(sA + j * A_SUB + (wm0 + tr) * BK, tr,
-                                  sA + A_FLOATS + j * BK * BN + wn0 + 4 * tc, acc);
+                compute_ktile<BN, (KSUB == 2 || LOADER != kLoaderTma) ? kOrderColumnSnake
+                                                                      : kOrderHalfSnake>(
+                    sA + j * A_SUB + (wm0 + tr) * BK, tr, sA + A_FLOATS + j * BK * BN + wn0 + 4 * tc,
+                    acc);
             if (LOADER == kLoaderTma) {
                 __syncthreads();  // every warp is done with stage s
                 if (s_abort) break;
