@@ -878,7 +878,16 @@ int device_sms(int dev) {
     return sms;
 }
 
-constexpr int kMinItersPerCta = 4;
+// k-tiles per CTA when a grid of under one wave splits every tile along K. Each CTA
+// computes c k-tiles; a tile's owner then adds the partial sums of the other
+// ceil(KT / c) - 1 pieces, and reading one piece (64 KiB per warp, from L2) costs about a
+// fifth of a 32-wide k-tile of paired FMAs, so c near sqrt(KT / (5 * KSUB)) minimises
+// c + (KT / c) / (5 * KSUB). (128^3: 1 k-tile per CTA on 4 SMs instead of all 4 on one.)
+int sk_min_iters_per_cta(long long KT, int KSUB) {
+    int c = 1;
+    while (static_cast<long long>(c + 1) * (c + 1) * 5 * KSUB <= KT) ++c;
+    return c;
+}
 
 template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG = 255,
           int LOADER = kLoaderTma, int KSUB = 1>
@@ -962,8 +971,8 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
         if (dp_tiles > 0) {
             G = g_full;
         } else {
-            // at least kMinItersPerCta k-tiles per CTA, never more CTAs than fit at once
-            G = sk_iters / kMinItersPerCta;
+            // never more CTAs than fit at once
+            G = sk_iters / sk_min_iters_per_cta(KT, KSUB);
             if (G > g_full) G = g_full;
             if (G < 1) G = 1;
         }
@@ -1212,8 +1221,8 @@ cudaError_t simt_launch_noalloc(const SimtProblem &p, cudaStream_t stream, const
         if (dp_tiles > 0) {
             G = g_full;
         } else {
-            // at least kMinItersPerCta k-tiles per CTA, never more CTAs than fit at once
-            G = sk_iters / kMinItersPerCta;
+            // never more CTAs than fit at once
+            G = sk_iters / sk_min_iters_per_cta(KT, 1);
             if (G > g_full) G = g_full;
             if (G < 1) G = 1;
         }

@@ -8,7 +8,7 @@ from __future__ import annotations
 SMS = 152
 
 # class name -> (representative (M, N, K) shapes, candidate configuration names)
-ALIGNED = ["dp_tma_128x128_s3", "dp_tma_128x256_s4", "sk_tma_ws_128x256_s4",
+ALIGNED = ["dp_tma_128x128_s3", "dp_tma_128x256_s4", "sk_tma_ws_128x128_s3", "sk_tma_ws_128x256_s4",
            "sk_tma_ws_256x128_s4", "pdp_tma_ws_128x256_s4", "sk_tma_ws_128x256_k64_s2",
            "sk_tma_ws_256x128_k64_s2"]
 UNALIGNED = ["packed_sk_tma_128x256_s4", "packed_dp_tma_128x128_s3", "packed_sk_tma_256x128_k64_s2",
