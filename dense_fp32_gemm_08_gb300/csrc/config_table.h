@@ -1,23 +1,14 @@
 // config_table.h: per-shape-class choice of SIMT kernel configuration.
 //
-// The winner of each shape class is measured (tuning/sweep.py) and written into
-// config_table_gen.h by tuning/gen_table.py at build time. Earlier hand sweeps that shaped the
-// classes (bench.py with SGEMM_FORCE_CONFIG, one configuration at a time, GB300, 152 SMs):
-//
-//   class                       measured                                         choice
-//   aligned, <  6 waves of       4096^3: sk 128x256 63.6 TF/s, dp 128x128 62.0,   sk_tma_ws_128x256_s4
-//     128x128 tiles at 2/SM      dp 128x256 54.5; 2048^3: sk 128x256 60.5,
-//                                dp 128x128 48.2, dp 128x256 53.0
-//   aligned, >= 6 waves          8192^3: dp 128x128 65.2, sk 128x256 64.1;         dp_tma_128x128_s3
-//                                16384x12288x4096: dp 128x128 65.3, sk 62.7
-//   aligned, one tile or less    256^3 and below: latency bound, a single          dp_tma_128x128_s3
-//                                128x128 CTA per tile has the shortest chain
-//   unaligned (no TMA)           4095x3001x1537: dp cp.async 128x256 30.1 TF/s,    packed_sk_tma_128x256_s4
-//                                sk cp.async 128x256 35.2; 127x129x4099: dp        (packed_dp_tma_128x128_s3
-//                                cp.async 0.72 ms, sk cp.async 0.10 ms             at >= 6 waves)
-//   unaligned, broadcast batch   operands that cannot be repacked once             sk_cpasync_128x256_s4
-//   N <= 8 (any alignment)       4096x1x4096: tile kernels 0.55 ms (HBM-bound)     skinny_tall_n8
-//   M <= 8 (any alignment)       1x4096x4096: tile kernels 0.34 ms (HBM-bound)     skinny_wide_m8
+// Problems with one output dimension of at most 8 go to the HBM-streaming kernels (skinny_*).
+// The rest fall into eight classes: operands TMA can read in place (16-byte aligned rows) or
+// not, times the grid depth in waves of 128 x 128 tiles at two CTAs per SM on 152 SMs:
+// tiny (at most 512 x 512 output cells), under one wave, 1 to 6 waves, 6 waves or more. The
+// fastest configuration of each class is measured by tuning/sweep.py on representative shapes
+// (CUDA events, L2 flushed before every call) and written into config_table_gen.h by
+// tuning/gen_table.py at build time, with the measured means beside each winner. A winner
+// that cannot run a particular problem (e.g. a broadcast batch that cannot be repacked) falls
+// back to a configuration that can.
 #pragma once
 
 #include "config_table_gen.h"
@@ -68,7 +59,7 @@ inline double waves_128x128(const SimtProblem &p) {
 
 inline int shape_class(const SimtProblem &p, bool aligned) {
     const int base = aligned ? kAlignedTiny : kUnalignedTiny;
-    if (static_cast<long long>(p.M) * p.N * p.batch <= 128LL * 128) return base;
+    if (static_cast<long long>(p.M) * p.N * p.batch <= 512LL * 512) return base;
     const double w = waves_128x128(p);
     return base + (w < 1.0 ? 1 : w < 6.0 ? 2 : 3);
 }

@@ -75,11 +75,12 @@ enum InnerOrder : int {
 // One k-tile (32 k-steps) of outer products for one thread's 8 x 16 tile.
 //   a_base: sA + (wm0 + tr) * 32, row r of the thread tile is 8 * r rows further (256 floats).
 //   b_base: sB + wn0 + 4 * tc, chunk q of the thread tile is 16 * q floats further.
-template <int BN, int ORDER>
+// KG_UNROLL < 8 keeps the k loop rolled (compact code for latency-bound launches).
+template <int BN, int ORDER, int KG_UNROLL = BK / 4>
 __device__ __forceinline__ void compute_ktile(const float *__restrict__ a_base, int tr,
                                               const float *__restrict__ b_base,
                                               float2 (&acc)[8][8]) {
-#pragma unroll
+#pragma unroll KG_UNROLL
     for (int kg = 0; kg < BK / 4; ++kg) {
         float4 a[8];
         const int achunk = (kg ^ tr) << 2;
@@ -734,6 +735,7 @@ const SimtConfig kConfigs[] = {
     {"sk_tma_ws_128x256_k64_s2", 128, 256, 2, 4, 2, kLoaderTma, kScheduleStreamK},
     {"sk_tma_ws_256x128_k64_s2", 256, 128, 4, 2, 2, kLoaderTma, kScheduleStreamK},
     {"packed_sk_tma_256x128_k64_s2", 256, 128, 4, 2, 2, kLoaderTma, kScheduleStreamK},
+    {"splitk_cpasync_64x64", 64, 64, 1, 1, 2, kLoaderCpAsync, kScheduleDataParallel},
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 
@@ -1023,6 +1025,7 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
 }
 
 bool packable(const SimtProblem &p);
+cudaError_t launch_small_splitk(const SimtProblem &p, cudaStream_t stream, const char **detail);
 cudaError_t launch_packed(int inner, const SimtProblem &p, cudaStream_t stream,
                           const char **detail);
 
@@ -1070,6 +1073,7 @@ cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const
             return launch_persistent<256, 128, 4, 2, 2, 255, kLoaderTma, 2>(kScheduleStreamK, p,
                                                                            stream, detail);
         case 18: return launch_packed(17, p, stream, detail);
+        case 19: return launch_small_splitk(p, stream, detail);
         default: *detail = "unknown SIMT configuration"; return cudaErrorInvalidValue;
     }
 }
@@ -1335,8 +1339,12 @@ std::vector<PackWorkspace> g_pack_ws;
 
 constexpr int kSlotTransposed = 0;
 constexpr int kSlotRealigned = 1;
+constexpr int kSlotSplitK = 2;
 
-cudaError_t pack_workspace(int dev, cudaStream_t stream, int slot, size_t bytes, float **out) {
+// *fresh (when given) reports a new allocation, whose contents are undefined.
+cudaError_t pack_workspace(int dev, cudaStream_t stream, int slot, size_t bytes, float **out,
+                           bool *fresh = nullptr) {
+    if (fresh) *fresh = false;
     std::lock_guard<std::mutex> lock(g_pack_mutex);
     PackWorkspace *e = nullptr;
     for (auto &w : g_pack_ws)
@@ -1358,6 +1366,7 @@ cudaError_t pack_workspace(int dev, cudaStream_t stream, int slot, size_t bytes,
             return err;
         }
         e->bytes = bytes;
+        if (fresh) *fresh = true;
     }
     *out = static_cast<float *>(e->ptr);
     return cudaSuccess;
@@ -1366,6 +1375,187 @@ cudaError_t pack_workspace(int dev, cudaStream_t stream, int slot, size_t bytes,
 bool packable(const SimtProblem &p) {
     // a broadcast operand (batch stride 0) would need one copy per batch entry: not packed
     return p.batch <= 1 || (p.strideA != 0 && p.strideB != 0);
+}
+
+// ---- small problems: one warp per 64 x 64 tile, K split over CTAs ------------------------
+//
+// For problems of a few tiles the large kernels leave most SMs idle and spend their time on
+// cold instruction fetch of a fully unrolled loop. Here each CTA is one warp computing a
+// 64 x 64 tile (the same 8 x 16 thread tile and fragment layout) over a slice of K, from a
+// two-stage cp.async ring (any alignment) and a rolled k loop. With more than one slice each
+// CTA stores its partial tile, and the CTA that finishes a tile last (an atomic count per
+// tile; nothing waits) adds the slices in slice order and applies the epilogue, so results
+// do not depend on which CTA finishes when; it then resets the count for the next call.
+
+struct SmallParams {
+    KParams k;
+    int split;                // K slices per tile
+    int kt_per_slice;         // 32-wide k-tiles per slice
+    float4 *partials;         // [tile][slice][32 x 32 float4]
+    unsigned int *counters;   // [tile]: slices finished
+};
+
+constexpr int kSmallStageFloats = 64 * BK + BK * 64;
+
+__global__ void __launch_bounds__(32) small_splitk_kernel(const SmallParams sp) {
+    const KParams &p = sp.k;
+    __shared__ __align__(16) float smem[2][kSmallStageFloats];
+    const int lane = threadIdx.x;
+    const int tile = blockIdx.x, slice = blockIdx.y;
+    const int tiles_per_batch = p.tiles_m * p.tiles_n;
+    const int b = tile / tiles_per_batch;
+    int tm, tn;
+    tile_coords(tile - b * tiles_per_batch, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    const int m0 = tm * 64, n0 = tn * 64;
+    const int KT = (p.K + BK - 1) / BK;
+    const int kt0 = slice * sp.kt_per_slice;
+    const int kt1 = min(KT, kt0 + sp.kt_per_slice);
+    const float *Ab = p.A + static_cast<long long>(b) * p.sA;
+    const float *Bb = p.B + static_cast<long long>(b) * p.sB;
+    const int tr = lane >> 2, tc = lane & 3;
+
+    float2 acc[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
+
+    if (kt0 < kt1)
+        cp_async_stage<64, 64, 32>(smem[0], smem[0] + 64 * BK, p, Ab, Bb, m0, n0, kt0 * BK, lane);
+    cp_async_commit();
+#pragma unroll 1
+    for (int kt = kt0; kt < kt1; ++kt) {
+        const int s = (kt - kt0) & 1;
+        if (kt + 1 < kt1)
+            cp_async_stage<64, 64, 32>(smem[s ^ 1], smem[s ^ 1] + 64 * BK, p, Ab, Bb, m0, n0,
+                                       (kt + 1) * BK, lane);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncwarp();  // k-tile kt landed for the whole warp
+        compute_ktile<64, kOrderHalfSnake, 1>(smem[s] + tr * BK, tr, smem[s] + 64 * BK + 4 * tc,
+                                              acc);
+        __syncwarp();  // stage s is free for the load two k-tiles ahead
+    }
+    cp_async_wait<0>();
+
+    float *Cb = p.C + static_cast<long long>(b) * p.sC;
+    if (sp.split == 1) {
+        epilogue(p, Cb, m0 + tr, n0 + 4 * tc, acc);
+        return;
+    }
+    float4 *mine = sp.partials + (static_cast<size_t>(tile) * sp.split + slice) * 1024;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int r = j >> 2, q = j & 3;
+        mine[j * 32 + lane] = make_float4(acc[r][2 * q].x, acc[r][2 * q].y, acc[r][2 * q + 1].x,
+                                          acc[r][2 * q + 1].y);
+    }
+    __threadfence();
+    __syncwarp();
+    unsigned int done = 0;
+    if (lane == 0) done = atomicAdd(&sp.counters[tile], 1u);
+    done = __shfl_sync(0xffffffffu, done, 0);
+    if (done != static_cast<unsigned int>(sp.split - 1)) return;  // not the last slice to finish
+    __threadfence();
+    const float4 *base = sp.partials + static_cast<size_t>(tile) * sp.split * 1024;
+#pragma unroll 1
+    for (int sl = 0; sl < sp.split; ++sl) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int r = j >> 2, q = j & 3;
+            const float4 v = __ldcg(base + static_cast<size_t>(sl) * 1024 + j * 32 + lane);
+            if (sl == 0) {
+                acc[r][2 * q] = make_float2(v.x, v.y);
+                acc[r][2 * q + 1] = make_float2(v.z, v.w);
+            } else {
+                acc[r][2 * q].x += v.x;
+                acc[r][2 * q].y += v.y;
+                acc[r][2 * q + 1].x += v.z;
+                acc[r][2 * q + 1].y += v.w;
+            }
+        }
+    }
+    if (lane == 0) sp.counters[tile] = 0u;  // ready for the next launch on this stream
+    epilogue(p, Cb, m0 + tr, n0 + 4 * tc, acc);
+}
+
+cudaError_t launch_small_splitk(const SimtProblem &p, cudaStream_t stream, const char **detail) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) {
+        *detail = "cudaGetDevice failed";
+        return err;
+    }
+    SmallParams sp;
+    KParams &kp = sp.k;
+    kp.M = p.M;
+    kp.N = p.N;
+    kp.K = p.K;
+    kp.alpha = p.alpha;
+    kp.beta = p.beta;
+    kp.A = p.A;
+    kp.B = p.B;
+    kp.C = p.C;
+    kp.lda = p.lda;
+    kp.ldb = p.ldb;
+    kp.ldc = p.ldc;
+    kp.sA = p.strideA;
+    kp.sB = p.strideB;
+    kp.sC = p.strideC;
+    kp.batch = p.batch;
+    kp.tiles_m = (p.M + 63) / 64;
+    kp.tiles_n = (p.N + 63) / 64;
+    kp.group_m = 8;
+    kp.a_vec4 = operand_vec4(p.A, p.lda, p.strideA, p.batch);
+    kp.b_vec4 = operand_vec4(p.B, p.ldb, p.strideB, p.batch);
+    kp.c_vec4 = operand_vec4(p.C, p.ldc, p.strideC, p.batch);
+    kp.bias = p.bias;
+    kp.act = p.act;
+    const long long tiles = static_cast<long long>(kp.tiles_m) * kp.tiles_n * p.batch;
+    if (tiles > 0x7fffffffLL) {
+        *detail = "too many output tiles for the split-K grid";
+        return cudaErrorInvalidValue;
+    }
+    // Slices: enough one-warp CTAs for about four per SM, at most 16 and at most one per
+    // 32-wide k-tile; then no empty slice.
+    const long long KT = (p.K + BK - 1) / BK;
+    const int sms = std::max(1, device_sms(dev));
+    long long split = (4LL * sms + tiles - 1) / tiles;
+    split = std::min<long long>(std::min<long long>(split, 16), std::max<long long>(KT, 1));
+    if (split < 1) split = 1;
+    const long long per = (KT + split - 1) / split;
+    split = per > 0 ? (KT + per - 1) / per : 1;
+    if (split < 1) split = 1;
+    sp.split = static_cast<int>(split);
+    sp.kt_per_slice = static_cast<int>(per > 0 ? per : 1);
+    sp.partials = nullptr;
+    sp.counters = nullptr;
+    if (split > 1) {
+        const size_t counter_bytes = (static_cast<size_t>(tiles) * 4 + 255) / 256 * 256;
+        const size_t bytes = counter_bytes + static_cast<size_t>(tiles) * split * 1024 * sizeof(float4);
+        float *ws = nullptr;
+        bool fresh = false;
+        err = pack_workspace(dev, stream, kSlotSplitK, bytes, &ws, &fresh);
+        if (err != cudaSuccess) {
+            *detail = "split-K workspace allocation failed";
+            return err;
+        }
+        if (fresh) {
+            // every count starts at zero; the last slice of each tile resets its count
+            err = cudaMemsetAsync(ws, 0, bytes, stream);
+            if (err != cudaSuccess) {
+                *detail = "split-K workspace initialisation failed";
+                return err;
+            }
+        }
+        sp.counters = reinterpret_cast<unsigned int *>(ws);
+        sp.partials = reinterpret_cast<float4 *>(reinterpret_cast<char *>(ws) + counter_bytes);
+    }
+    small_splitk_kernel<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(split)), 32, 0,
+                          stream>>>(sp);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) *detail = "kernel launch failed";
+    return err;
 }
 
 cudaError_t launch_packed(int inner, const SimtProblem &p, cudaStream_t stream,

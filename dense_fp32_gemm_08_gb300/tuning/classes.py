@@ -10,17 +10,17 @@ SMS = 152
 # class name -> (representative (M, N, K) shapes, candidate configuration names)
 ALIGNED = ["dp_tma_128x128_s3", "dp_tma_128x256_s4", "sk_tma_ws_128x128_s3", "sk_tma_ws_128x256_s4",
            "sk_tma_ws_256x128_s4", "pdp_tma_ws_128x256_s4", "sk_tma_ws_128x256_k64_s2",
-           "sk_tma_ws_256x128_k64_s2"]
+           "sk_tma_ws_256x128_k64_s2", "splitk_cpasync_64x64"]
 UNALIGNED = ["packed_sk_tma_128x256_s4", "packed_dp_tma_128x128_s3", "packed_sk_tma_256x128_k64_s2",
              "sk_cpasync_128x256_s4",
-             "dp_cpasync_128x256_s4", "dp_cpasync_128x128_s3"]
+             "dp_cpasync_128x256_s4", "dp_cpasync_128x128_s3", "splitk_cpasync_64x64"]
 
 CLASSES = {
-    "aligned_tiny": ([(96, 96, 512), (128, 64, 2048)], ALIGNED),
-    "aligned_small": ([(512, 512, 512), (1024, 1024, 1024), (2048, 2048, 2048)], ALIGNED),
+    "aligned_tiny": ([(128, 128, 128), (256, 256, 256), (512, 512, 512), (128, 64, 2048)], ALIGNED),
+    "aligned_small": ([(1024, 1024, 1024), (1024, 2048, 1024), (2048, 2048, 2048)], ALIGNED),
     "aligned_medium": ([(4096, 4096, 4096), (4096, 3072, 2048), (3072, 4096, 4096)], ALIGNED),
     "aligned_large": ([(8192, 8192, 8192), (16384, 12288, 4096)], ALIGNED),
-    "unaligned_tiny": ([(97, 95, 513), (127, 129, 4099)], UNALIGNED),
+    "unaligned_tiny": ([(97, 95, 513), (127, 129, 4099), (255, 257, 253), (511, 509, 515)], UNALIGNED),
     "unaligned_small": ([(1001, 999, 1003), (2047, 2045, 2049)], UNALIGNED),
     "unaligned_medium": ([(4095, 3001, 1537), (4097, 4093, 4099)], UNALIGNED),
     "unaligned_large": ([(8191, 8193, 8195)], UNALIGNED),
@@ -36,7 +36,7 @@ def waves(M: int, N: int, batch: int = 1) -> float:
 def classify(M: int, N: int, aligned: bool, batch: int = 1) -> str:
     """The class of a problem (mirrors table_choose in config_table.h)."""
     prefix = "aligned" if aligned else "unaligned"
-    if M * N * batch <= 128 * 128:
+    if M * N * batch <= 512 * 512:
         return prefix + "_tiny"
     w = waves(M, N, batch)
     if w < 1.0:

@@ -195,6 +195,27 @@ def test_stream_k_deterministic_and_exact(sg, name):
         sg.sgemm_force_config(-1)
 
 
+def test_small_splitk_deterministic_and_exact(sg):
+    """The one-warp split-K kernel: several K slices per tile, the last to finish adds them in
+    slice order, so repeated runs agree bit for bit; small integers are exact."""
+    ids = {sg.sgemm_config_name(i): i for i in range(sg.sgemm_num_configs())}
+    sg.sgemm_force_config(ids["splitk_cpasync_64x64"])
+    try:
+        for M, N, K in [(256, 256, 4096), (200, 130, 1000), (64, 64, 32), (1, 70, 3000)]:
+            case = Case(M, N, K, 0.7, -1.3, "normal", seed=M + K)
+            err, first, _ = run(case, sg.sgemm, torch)
+            assert err <= TOL
+            _, second, _ = run(case, sg.sgemm, torch, check=False)
+            assert np.array_equal(first, second), "split-K result differs between runs"
+            got, ref = _check(Case(M, N, K, 1.0, -1.0, "small_int", seed=M + N), sg)
+            assert np.array_equal(got, ref)
+        # unaligned operands and a batch
+        _check(Case(333, 291, 457, 0.7, -1.3, "normal", seed=7, lda_pad=1, ldb_pad=2, ldc_pad=3,
+                    a_off=1, b_off=2, c_off=3), sg)
+    finally:
+        sg.sgemm_force_config(-1)
+
+
 # ---- strided batched ----------------------------------------------------------------------
 
 def _batched(sg, M, N, K, batch, sA, sB, sC, alpha, beta, entry, exact=False):
