@@ -183,7 +183,8 @@ def test_force_config(sgemm_lib):
         tma_ids = [i for i in range(n) if sgemm_lib.sgemm_config_name(i).startswith(("dp_tma", "sk_tma"))]
         sgemm_lib.sgemm_force_config(tma_ids[0])
         got = sel(512, 512, 512, 1.0, FAKE + 4, 512, FAKE, 512, FAKE, 512)
-        assert sgemm_lib.sgemm_config_name(got).startswith(("packed", "dp_cpasync", "sk_cpasync"))
+        assert sgemm_lib.sgemm_config_name(got).startswith(("packed", "dp_cpasync", "sk_cpasync",
+                                                            "splitk_cpasync"))
         with pytest.raises(sgemm_lib.SgemmError):
             sgemm_lib.sgemm_force_config(n)
     finally:
