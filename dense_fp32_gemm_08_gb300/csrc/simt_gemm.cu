@@ -24,6 +24,12 @@
 //      ("float4" chapter: 128-bit loads), no transposed copy of A is needed.
 //  * Epilogue: alpha * acc + beta * C fused, float4 loads and stores where C allows,
 //    C never read when beta == 0.
+//  * Schedules: a data-parallel grid (one CTA per tile); a persistent grid (one CTA per SM,
+//    or two) that deals whole tiles round-robin and splits the last partial wave's tiles
+//    along K (stream-K, deterministic fixed-order fix-up); persistent variants whose stages
+//    hold two 32-wide k-tiles (one CTA barrier per 64 k-steps); and, for outputs of at most
+//    512 x 512, one warp per 64 x 64 tile with K split over CTAs. Which one runs is decided
+//    per shape class by measured sweeps (config_table.h).
 #include "epilogue.cuh"
 #include "ptx.cuh"
 #include "raster.cuh"

@@ -15,9 +15,11 @@
  * --------------------------------------
  * Memory and ownership: A, B and C are device pointers owned by the caller (for example
  *   torch CUDA tensors). The library keeps no reference to them after the call returns.
- *   No entry point allocates device memory per call. The stream-K split of the tile grid
- *   uses one workspace per device, allocated on first use and kept until
- *   sgemm_release_workspace().
+ *   No entry point allocates device memory on every call: workspaces are allocated on first
+ *   use (per device and stream: stream-K and split-K partial sums, repacked or transposed
+ *   operand copies, the 3xTF32 / TF32 split operands; per device: the host-memory path's
+ *   buffers), grown when a larger problem needs more, and kept until
+ *   sgemm_release_workspace(). sgemm_noalloc() uses none of them.
  * Streams: every compute call is asynchronous on `stream` (a cudaStream_t; NULL means the
  *   legacy default stream) and does not synchronise. Results are visible to later work on
  *   the same stream.
@@ -237,13 +239,15 @@ sgemm_status_t sgemm_fused_strided_batched(sgemm_op_t transa, sgemm_op_t transb,
 /*
  * The product with A, B and C in HOST memory (same sizes, leading dimensions, alpha / beta
  * rules and argument errors as sgemm()). The call returns when C holds the result. B is
- * uploaded once; the rows of A (and of C when beta != 0) travel in chunks of about M / 8
- * rows through two device buffers each, uploaded on an internal stream while the previous
- * chunk is computed on `stream` (the SIMT path) and the one before it is downloaded on
- * another internal stream. With pinned (page-locked) host memory the copies overlap the
- * computation; pageable memory works but the copies then serialise. Device buffers of
- * 4 * (K * N + 2 * chunk * (K + N)) bytes are kept per device until
- * sgemm_release_workspace(); calls on the same device run one at a time.
+ * uploaded once; the rows of A (and of C when beta != 0) travel in chunks (at least M / 8
+ * rows, grown until a chunk fills the GPU with tiles) through two device buffers each,
+ * uploaded on an internal stream while the previous chunk is computed on `stream` (the SIMT
+ * path) and the one before it is downloaded on another internal stream. The first chunk is
+ * computed in up to four K slices, each starting when its part of B has arrived (the slices
+ * accumulate in fp32, like stream-K pieces). With pinned (page-locked) host memory the copies
+ * overlap the computation; pageable memory works but the copies then serialise. Device
+ * buffers of about 4 * (K * N + 2 * chunk * (K + N)) bytes (rows padded to 16 bytes) are kept
+ * per device until sgemm_release_workspace(); calls on the same device run one at a time.
  */
 sgemm_status_t sgemm_host(int64_t M, int64_t N, int64_t K, float alpha,
                           const float *A, int64_t lda, const float *B, int64_t ldb,
@@ -273,8 +277,9 @@ sgemm_status_t sgemm_device_status(void *stream);
  */
 sgemm_status_t sgemm_selftest_bounded_wait(int which, void *stream);
 
-/* Frees the per-device workspaces: stream-K partial sums and 3xTF32 split operands (the
- * next call that needs one allocates it again). Synchronises the device first. */
+/* Frees every workspace: stream-K and split-K partial sums, repacked and transposed operand
+ * copies, TF32 split operands and the host-memory path's buffers (the next call that needs
+ * one allocates it again). Synchronises the device first. */
 sgemm_status_t sgemm_release_workspace(void);
 
 /*
