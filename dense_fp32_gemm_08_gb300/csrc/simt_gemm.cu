@@ -1345,7 +1345,8 @@ std::vector<PackWorkspace> g_pack_ws;
 
 constexpr int kSlotTransposed = 0;
 constexpr int kSlotRealigned = 1;
-constexpr int kSlotSplitK = 2;
+constexpr int kSlotSplitK = 2;        // split-K partial tiles
+constexpr int kSlotSplitKCount = 3;   // split-K per-tile counts (zero between launches)
 
 // *fresh (when given) reports a new allocation, whose contents are undefined.
 cudaError_t pack_workspace(int dev, cudaStream_t stream, int slot, size_t bytes, float **out,
@@ -1537,25 +1538,23 @@ cudaError_t launch_small_splitk(const SimtProblem &p, cudaStream_t stream, const
     sp.partials = nullptr;
     sp.counters = nullptr;
     if (split > 1) {
-        const size_t counter_bytes = (static_cast<size_t>(tiles) * 4 + 255) / 256 * 256;
-        const size_t bytes = counter_bytes + static_cast<size_t>(tiles) * split * 1024 * sizeof(float4);
-        float *ws = nullptr;
+        // The counts live in their own allocation: zeroed whenever it is (re)allocated, and
+        // left at zero by every launch (the last slice of each tile resets its count), so any
+        // later launch on this stream, of any tile count that fits, starts from zeros.
+        float *cnt = nullptr, *ws = nullptr;
         bool fresh = false;
-        err = pack_workspace(dev, stream, kSlotSplitK, bytes, &ws, &fresh);
+        const size_t count_bytes = static_cast<size_t>(tiles) * sizeof(unsigned int);
+        err = pack_workspace(dev, stream, kSlotSplitKCount, count_bytes, &cnt, &fresh);
+        if (err == cudaSuccess && fresh) err = cudaMemsetAsync(cnt, 0, count_bytes, stream);
+        if (err == cudaSuccess)
+            err = pack_workspace(dev, stream, kSlotSplitK,
+                                 static_cast<size_t>(tiles) * split * 1024 * sizeof(float4), &ws);
         if (err != cudaSuccess) {
             *detail = "split-K workspace allocation failed";
             return err;
         }
-        if (fresh) {
-            // every count starts at zero; the last slice of each tile resets its count
-            err = cudaMemsetAsync(ws, 0, bytes, stream);
-            if (err != cudaSuccess) {
-                *detail = "split-K workspace initialisation failed";
-                return err;
-            }
-        }
-        sp.counters = reinterpret_cast<unsigned int *>(ws);
-        sp.partials = reinterpret_cast<float4 *>(reinterpret_cast<char *>(ws) + counter_bytes);
+        sp.counters = reinterpret_cast<unsigned int *>(cnt);
+        sp.partials = reinterpret_cast<float4 *>(ws);
     }
     small_splitk_kernel<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(split)), 32, 0,
                           stream>>>(sp);

@@ -209,9 +209,15 @@ def test_small_splitk_deterministic_and_exact(sg):
             assert np.array_equal(first, second), "split-K result differs between runs"
             got, ref = _check(Case(M, N, K, 1.0, -1.0, "small_int", seed=M + N), sg)
             assert np.array_equal(got, ref)
-        # unaligned operands and a batch
+        # unaligned operands
         _check(Case(333, 291, 457, 0.7, -1.3, "normal", seed=7, lda_pad=1, ldb_pad=2, ldc_pad=3,
                     a_off=1, b_off=2, c_off=3), sg)
+        # a launch with more tiles after one with more partial-tile storage (120 tiles in 6
+        # slices, then 130 tiles in 5): every tile's count must start at zero
+        _check(Case(640, 768, 544, 1.0, 0.0, "uniform", seed=21), sg)
+        got, ref = _check(Case(640, 832, 160, 1.0, -1.0, "small_int", seed=22), sg)
+        assert np.array_equal(got, ref)
+        _check(Case(640, 832, 160, 0.7, -1.3, "normal", seed=23), sg)
     finally:
         sg.sgemm_force_config(-1)
 
