@@ -196,3 +196,33 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path, sgemm_lib):
     monkeypatch.setattr(sgemm_lib, "_lib", None)
     with pytest.raises(RuntimeError):
         sgemm_lib.lib()
+
+
+class _FailingLibrary:
+    """Stands in for the loaded library: every product call fails the way a device-memory
+    shortage or a launch error would, with the library's own message."""
+
+    def __init__(self, status, message):
+        self.status, self.message = status, message
+
+    def __getattr__(self, name):
+        if name == "sgemm_last_error":
+            return lambda: self.message
+        if name == "sgemm_status_string":
+            return lambda status: b"SGEMM_ERR_LAUNCH"
+        return lambda *args: self.status
+
+
+@pytest.mark.parametrize("status,message", [
+    (2, b"split-K workspace allocation failed: out of memory"),
+    (2, b"kernel launch failed: invalid configuration argument"),
+    (3, b""),
+])
+def test_binding_raises_the_library_error(monkeypatch, sgemm_lib, status, message):
+    monkeypatch.setattr(sgemm_lib, "_lib", _FailingLibrary(status, message))
+    with pytest.raises(sgemm_lib.SgemmError) as info:
+        sgemm_lib.sgemm(4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4)
+    assert info.value.status == status
+    assert (message.decode() or "SGEMM_ERR_LAUNCH") in str(info.value)
+    with pytest.raises(sgemm_lib.SgemmError):
+        sgemm_lib.sgemm_3xtf32(4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4)
