@@ -79,9 +79,8 @@ def test_invalid_arguments(sgemm_lib, args, why):
 
 def test_ex_argument_rules(sgemm_lib):
     L = sgemm_lib.lib()
-    # transposed A: lda >= M; transposed B: ldb >= K
-    ok_t = (1, 1, 0, 8, 6, 4, 1.0, FAKE, 8, FAKE, 4, 0.0, FAKE, 6, None)
-    assert L.sgemm_ex(*ok_t) != sgemm_lib.SGEMM_ERR_INVALID_VALUE
+    # transposed A needs lda >= M, transposed B ldb >= K (the accepted minimum is exercised
+    # on real device buffers in test_gpu_trans.py: a valid call here would launch kernels)
     bad_lda = (1, 0, 0, 8, 6, 4, 1.0, FAKE, 7, FAKE, 6, 0.0, FAKE, 6, None)
     assert L.sgemm_ex(*bad_lda) == sgemm_lib.SGEMM_ERR_INVALID_VALUE
     assert "transposed" in L.sgemm_last_error().decode()
