@@ -18,7 +18,10 @@ Sources of each pin:
 * transposes: stored transposes through the ex entry agree with the plain product on
   numpy-transposed copies, with exact rational brute force, and with identity products.
 * fused epilogue: each activation against its published formula evaluated with Python's
-  math module; bias and residual against exact integer sums; activation before residual.
+  math module; bias and residual against exact integer sums; activation before residual;
+  the same on all four operand forms, with the operands stored transposed.
+* denominators: sum_k |op(A)_ik| |op(B)_kj| on small integers equals numpy's int64 product of
+  the absolute values of numpy-transposed copies, for all four operand forms.
 * brute force: exact rational arithmetic (fractions.Fraction) on tiny shapes, rounded once
   to fp32; the oracle may differ by at most one fp32 ulp (its fp64 sum rounds before the
   final rounding).
@@ -295,6 +298,89 @@ def pin_epilogue_bias_and_residual(lib):
     return np.array_equal(got, want)
 
 
+def _op_storage(X, trans, pad):
+    """Storage of op(X) = X: X itself or its transpose, with `pad` columns of NaN padding."""
+    s = np.ascontiguousarray(X.T) if trans else X
+    ld = s.shape[1] + pad
+    return synth.padded(s, ld, np.nan), ld
+
+
+def pin_absdot(lib):
+    # sum_k |op(A)_ik| |op(B)_kj| on small integers (all partial sums exact) against numpy's
+    # int64 product of the absolute values; the stored operands carry padding between rows,
+    # and A, B are not square, so a transposed index or a dropped absolute value shows.
+    M, N, K = 7, 9, 33
+    A = synth.small_int(M, K, 91)
+    B = synth.small_int(K, N, 92)
+    want = (np.abs(A).astype(np.int64) @ np.abs(B).astype(np.int64)).astype(np.float64)
+    for ta in (False, True):
+        for tb in (False, True):
+            As, lda = _op_storage(A, ta, 3)
+            Bs, ldb = _op_storage(B, tb, 2)
+            As = np.where(np.isnan(As), 0.0, As).astype(np.float32)
+            Bs = np.where(np.isnan(Bs), 0.0, Bs).astype(np.float32)
+            got = oracle.absdot_ex(ta, tb, M, N, K, As, lda, Bs, ldb, lib=lib)
+            if not np.array_equal(got, want):
+                return False
+            rows = [6, 0, 3]
+            if not np.array_equal(oracle.absdot_ex(ta, tb, M, N, K, As, lda, Bs, ldb, rows=rows,
+                                                   lib=lib), want[rows]):
+                return False
+    Ap, Bp = synth.padded(A, K + 3, 0.0), synth.padded(B, N + 2, 0.0)
+    return np.array_equal(oracle.absdot(M, N, K, Ap, K + 3, Bp, N + 2, lib=lib), want)
+
+
+def pin_epilogue_transposed(lib):
+    # (1) act = none and relu on exact small integers, every operand form, stored transposes
+    # with padding: act(2 S + bias) + 3 C equals the int64 value exactly.
+    M, N, K = 6, 10, 21
+    A, B, C = synth.small_int(M, K, 93), synth.small_int(K, N, 94), synth.small_int(M, N, 95)
+    bias = synth.small_int(1, N, 96).reshape(-1)
+    S = A.astype(np.int64) @ B.astype(np.int64)
+    pre = 2 * S + bias.astype(np.int64)[None, :]
+    for ta in (False, True):
+        for tb in (False, True):
+            As, lda = _op_storage(A, ta, 1)
+            Bs, ldb = _op_storage(B, tb, 4)
+            As = np.where(np.isnan(As), 0.0, As).astype(np.float32)
+            Bs = np.where(np.isnan(Bs), 0.0, Bs).astype(np.float32)
+            for act, f in (("none", lambda v: v), ("relu", lambda v: np.maximum(v, 0))):
+                want = (f(pre) + 3 * C.astype(np.int64)).astype(np.float32)
+                got = oracle.sgemm_epilogue(ta, tb, M, N, K, 2.0, As, lda, Bs, ldb, 3.0, C, N,
+                                            bias, act, lib=lib)
+                if not np.array_equal(got, want):
+                    return False
+    # (2) each activation through transposed storage: op(A) has the chosen values xs in its
+    # first column and zeros elsewhere, op(B) ones in its first row, so every cell of row i
+    # is act(xs[i]); compared with the formula evaluated by Python's math module.
+    import math
+    xs = np.array([-6.0, -2.5, -1.0, -0.25, 0.0, 0.5, 1.0, 3.0, 7.5], np.float32)
+    n, Kx, Nx = len(xs), 3, 4
+    A2 = np.zeros((n, Kx), np.float32)
+    A2[:, 0] = xs
+    B2 = np.zeros((Kx, Nx), np.float32)
+    B2[0, :] = 1.0
+    forms = {
+        "gelu": lambda x: 0.5 * x * (1.0 + math.erf(x / math.sqrt(2.0))),
+        "gelu_tanh": lambda x: 0.5 * x * (1.0 + math.tanh(math.sqrt(2.0 / math.pi) *
+                                                          (x + 0.044715 * x ** 3))),
+        "silu": lambda x: x / (1.0 + math.exp(-x)),
+    }
+    for ta in (False, True):
+        for tb in (False, True):
+            As, lda = _op_storage(A2, ta, 2)
+            Bs, ldb = _op_storage(B2, tb, 1)
+            As = np.where(np.isnan(As), 0.0, As).astype(np.float32)
+            Bs = np.where(np.isnan(Bs), 0.0, Bs).astype(np.float32)
+            for act, f in forms.items():
+                got = oracle.sgemm_epilogue(ta, tb, n, Nx, Kx, 1.0, As, lda, Bs, ldb, 0.0, None,
+                                            Nx, None, act, lib=lib)
+                want = np.array([[np.float32(f(float(x)))] * Nx for x in xs], np.float32)
+                if not np.array_equal(got, want):
+                    return False
+    return True
+
+
 PINS = {
     "identity": pin_identity,
     "permutation": pin_permutation,
@@ -310,4 +396,6 @@ PINS = {
     "transposed_brute_force": pin_transposed_brute_force,
     "epilogue_activations": pin_epilogue_activations,
     "epilogue_bias_and_residual": pin_epilogue_bias_and_residual,
+    "epilogue_transposed": pin_epilogue_transposed,
+    "absdot": pin_absdot,
 }

@@ -24,26 +24,31 @@ def test_pin(name, oracle_lib):
 MUTANTS = {
     "dropped_beta_term": ("if (beta != 0.0) v += beta * (double)C[i * ldc + j];",
                           "(void)beta;"),
-    "transposed_B": ("acc[j] += a * (double)brow[j];",
-                     "acc[j] += a * (double)B[j * ldb + k];"),
-    "transposed_A": ("const double a = (double)A[i * lda + k];",
-                     "const double a = (double)A[k * lda + i];"),
+    "transposed_B": ("    s.bk = transb ? 1 : ldb;\n    s.bj = transb ? ldb : 1;",
+                     "    s.bk = transb ? ldb : 1;\n    s.bj = transb ? 1 : ldb;"),
+    "transposed_A": ("    s.ai = transa ? 1 : lda;\n    s.ak = transa ? lda : 1;",
+                     "    s.ai = transa ? lda : 1;\n    s.ak = transa ? 1 : lda;"),
     "dropped_last_k": ("for (int64_t k = 0; k < K; ++k) {\n                    const double a = (double)A",
                        "for (int64_t k = 0; k + 1 < K; ++k) {\n                    const double a = (double)A"),
     "alpha_sign": ("double v = (alpha != 0.0) ? alpha * acc[j] : 0.0;",
                    "double v = (alpha != 0.0) ? -alpha * acc[j] : 0.0;"),
     "beta_zero_reads_C": ("if (beta != 0.0) v += beta * (double)C[i * ldc + j];",
                           "v += beta * (double)C[i * ldc + j];"),
-    "fp32_accumulator": ("acc[j] += a * (double)brow[j];",
-                         "acc[j] = (double)((float)acc[j] + (float)(a * (double)brow[j]));"),
+    "fp32_accumulator": ("acc[j] += a * (double)brow[j * st.bj];",
+                         "acc[j] = (double)((float)acc[j] + (float)(a * (double)brow[j * st.bj]));"),
     "alpha_scales_C": ("if (beta != 0.0) v += beta * (double)C[i * ldc + j];",
                        "if (beta != 0.0) v += alpha * beta * (double)C[i * ldc + j];"),
-    "ld_ignored": ("const float *brow = B + k * ldb;\n                    for (int64_t j = 0; j < N; ++j) acc[j] += a",
-                   "const float *brow = B + k * N;\n                    for (int64_t j = 0; j < N; ++j) acc[j] += a"),
-    "ex_transposed_A_index": ("const double a = (double)(transa ? A[k * lda + i] : A[i * lda + k]);",
-                              "const double a = (double)(transa ? A[i * lda + k] : A[i * lda + k]);"),
-    "ex_transposed_B_index": ("acc[j] += a * (double)(transb ? B[j * ldb + k] : B[k * ldb + j]);",
-                              "acc[j] += a * (double)(transb ? B[k * ldb + j] : B[k * ldb + j]);"),
+    "ldc_ignored": ("if (beta != 0.0) v += beta * (double)C[i * ldc + j];",
+                    "if (beta != 0.0) v += beta * (double)C[i * N + j];"),
+    "lda_for_ldb": ("    s.bk = transb ? 1 : ldb;", "    s.bk = transb ? 1 : lda;"),
+    "ex_transposed_A_index": ("    s.ai = transa ? 1 : lda;\n    s.ak = transa ? lda : 1;",
+                              "    s.ai = lda;\n    s.ak = 1;"),
+    "ex_transposed_B_index": ("    s.bk = transb ? 1 : ldb;\n    s.bj = transb ? ldb : 1;",
+                              "    s.bk = ldb;\n    s.bj = 1;"),
+    "ex_ignores_transpose": ("return product_rows(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, NULL, 0,",
+                             "return product_rows(0, 0, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, NULL, 0,"),
+    "epilogue_ignores_transpose": ("return product_rows(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act,",
+                                   "return product_rows(0, 0, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, act,"),
     "epilogue_gelu_constant": ("return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
                                "return 0.5 * x * (1.0 + erf(x / 2.0));"),
     "epilogue_act_after_residual": ("                v = activation(v, act);\n                if (beta != 0.0) v += beta * (double)C[i * ldc + j];",
@@ -51,6 +56,16 @@ MUTANTS = {
     "epilogue_bias_dropped": ("if (bias) v += (double)bias[j];", "(void)bias;"),
     "wrong_row_index": ("const int64_t i = rows ? rows[r] : r;\n            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;",
                         "const int64_t i = r;\n            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;"),
+    "absdot_dropped_abs_A": ("const double a = fabs((double)A[i * st.ai + k * st.ak]);",
+                             "const double a = (double)A[i * st.ai + k * st.ak];"),
+    "absdot_dropped_abs_B": ("drow[j] += a * fabs((double)brow[j * st.bj]);",
+                             "drow[j] += a * (double)brow[j * st.bj];"),
+    "absdot_ignores_transpose": ("    const op_strides st = strides_of(transa, transb, lda, ldb);\n#pragma omp parallel for",
+                                 "    const op_strides st = strides_of(0, 0, lda, ldb);\n#pragma omp parallel for"),
+    "absdot_wrong_row_index": ("const int64_t i = rows ? rows[r] : r;\n        double *drow",
+                               "const int64_t i = r;\n        double *drow"),
+    "absdot_plain_transposes": ("return sgemm_ref_absdot_ex_rows(0, 0, M,",
+                                "return sgemm_ref_absdot_ex_rows(0, 1, M,"),
 }
 
 
@@ -81,7 +96,7 @@ print("FAILED_PINS", ",".join(failed))
 def test_pins_catch_mutant(name, mutant_dir):
     src = oracle.SOURCE.read_text()
     old, new = MUTANTS[name]
-    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    assert src.count(old) == 1, f"mutation anchor for {name} must occur exactly once"
     path = mutant_dir / f"{name}.c"
     path.write_text(src.replace(old, new, 1))
     lib_path = oracle.build(path, mutant_dir / f"lib{name}.so")
