@@ -2,7 +2,8 @@
 //
 // Problems with one output dimension of at most 8 go to the HBM-streaming kernels (skinny_*).
 // The rest fall into eight classes: operands TMA can read in place (16-byte aligned rows) or
-// not, times the grid depth in waves of 128 x 128 tiles at two CTAs per SM on 152 SMs:
+// not, times the grid depth in waves of 128 x 128 tiles at two CTAs per SM on the device's
+// multiprocessors (read at run time; 152 on a GB300):
 // tiny (at most 512 x 512 output cells), under one wave, 1 to 6 waves, 6 waves or more. The
 // fastest configuration of each class is measured by tuning/sweep.py on representative shapes
 // (CUDA events, L2 flushed before every call) and written into config_table_gen.h by
@@ -51,16 +52,20 @@ enum ShapeClass : int {
     kUnalignedLarge,
 };
 
-// Waves of 128 x 128 tiles at two CTAs per SM on a 152-SM part.
-inline double waves_128x128(const SimtProblem &p) {
+// Multiprocessors assumed when no device can be queried (a host-only configuration query):
+// the GB300's count.
+constexpr int kDefaultSms = 152;
+
+// Waves of 128 x 128 tiles at two CTAs per SM on a part with `sms` multiprocessors.
+inline double waves_128x128(const SimtProblem &p, int sms) {
     const double tiles = static_cast<double>((p.M + 127) / 128) * ((p.N + 127) / 128) * p.batch;
-    return tiles / (2.0 * 152.0);
+    return tiles / (2.0 * (sms > 0 ? sms : kDefaultSms));
 }
 
-inline int shape_class(const SimtProblem &p, bool aligned) {
+inline int shape_class(const SimtProblem &p, bool aligned, int sms) {
     const int base = aligned ? kAlignedTiny : kUnalignedTiny;
     if (static_cast<long long>(p.M) * p.N * p.batch <= 512LL * 512) return base;
-    const double w = waves_128x128(p);
+    const double w = waves_128x128(p, sms);
     return base + (w < 1.0 ? 1 : w < 6.0 ? 2 : 3);
 }
 
@@ -74,20 +79,20 @@ inline int config_by_name(const char *name) {
     return -1;
 }
 
-// Picks the configuration id for a problem: the bandwidth kernels for skinny shapes, else
-// the measured winner of the problem's shape class (falling back to a configuration that
-// can run the problem when the winner cannot, e.g. a broadcast batch that cannot be
-// repacked).
-inline int table_choose(const SimtProblem &p) {
+// Picks the configuration id for a problem on a part with `sms` multiprocessors (0: unknown,
+// taken as kDefaultSms): the bandwidth kernels for skinny shapes, else the measured winner of
+// the problem's shape class (falling back to a configuration that can run the problem when
+// the winner cannot, e.g. a broadcast batch that cannot be repacked).
+inline int table_choose(const SimtProblem &p, int sms) {
     // One output dimension of at most 8: HBM-bound, the bandwidth kernels (any alignment).
     if (simt_config_supports(kCfgSkinnyTall, p)) return kCfgSkinnyTall;
     if (simt_config_supports(kCfgSkinnyWide, p)) return kCfgSkinnyWide;
     const bool tma = simt_config_supports(kCfgDpTma128x128, p);
-    const int cls = shape_class(p, tma);
+    const int cls = shape_class(p, tma, sms);
     const int id = config_by_name(kClassWinner[cls]);
     if (id >= 0 && simt_config_supports(id, p)) return id;
     if (tma) return kCfgSkTma128x256;
-    return waves_128x128(p) >= 6.0 ? kCfgDpCp128x128 : kCfgSkCp128x256;
+    return waves_128x128(p, sms) >= 6.0 ? kCfgDpCp128x128 : kCfgSkCp128x256;
 }
 
 }  // namespace sg

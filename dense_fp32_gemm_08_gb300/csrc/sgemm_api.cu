@@ -161,7 +161,7 @@ sg::SimtProblem to_problem(const Args &a) {
 int choose_simt(const sg::SimtProblem &p) {
     const int forced = forced_config();
     if (forced >= 0 && sg::simt_config_supports(forced, p)) return forced;
-    return sg::table_choose(p);
+    return sg::table_choose(p, sg::simt_device_sms());
 }
 
 sgemm_status_t run_simt(const Args &a, cudaStream_t stream) {

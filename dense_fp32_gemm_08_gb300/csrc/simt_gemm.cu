@@ -1039,6 +1039,15 @@ cudaError_t launch_packed(int inner, const SimtProblem &p, cudaStream_t stream,
 
 int simt_num_configs() { return kNumConfigs; }
 
+int simt_device_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();  // leave no sticky error for the caller
+        return 0;
+    }
+    return device_sms(dev);
+}
+
 const SimtConfig &simt_config(int id) { return kConfigs[id]; }
 
 bool simt_config_supports(int id, const SimtProblem &p) {

@@ -47,6 +47,10 @@ struct SimtProblem {
 };
 
 int simt_num_configs();
+
+// Multiprocessors of the calling thread's current device (queried once per device), or 0 when
+// there is no device to query.
+int simt_device_sms();
 const SimtConfig &simt_config(int id);
 
 // True when config `id` can run this problem (alignment needs of its loader).

@@ -204,7 +204,8 @@ cudaError_t launch_tall(const SkinnyProblem &p, cudaStream_t stream) {
     const bool vec = aligned16(p.A) && p.lda % 4 == 0 && (p.batch <= 1 || p.strideA % 4 == 0);
     const long long rows = static_cast<long long>(p.M) * p.batch;
     long long blocks = (rows + 7) / 8;
-    if (blocks > 152LL * 64) blocks = 152LL * 64;
+    const long long cap = 64LL * (simt_device_sms() > 0 ? simt_device_sms() : 152);
+    if (blocks > cap) blocks = cap;
     if (vec)
         skinny_tall_kernel<NN, true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
     else

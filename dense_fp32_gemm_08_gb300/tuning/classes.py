@@ -1,7 +1,8 @@
 """Shape classes of the configuration table, their representative shapes and candidates.
 
 A class is decided by the operands' TMA alignment and by the grid depth in waves of 128 x 128
-tiles at two CTAs per SM (152 SMs): the same rule `config_table.h` applies at run time.
+tiles at two CTAs per SM on the device's multiprocessors (152 on a GB300, the default here):
+the same rule `config_table.h` applies at run time with the count it reads from the device.
 The M <= 8 and N <= 8 shapes always take the bandwidth kernels and are not swept."""
 from __future__ import annotations
 
@@ -29,16 +30,17 @@ CLASSES = {
 CLASS_ORDER = list(CLASSES)
 
 
-def waves(M: int, N: int, batch: int = 1) -> float:
-    return ((M + 127) // 128) * ((N + 127) // 128) * batch / (2.0 * SMS)
+def waves(M: int, N: int, batch: int = 1, sms: int = SMS) -> float:
+    return ((M + 127) // 128) * ((N + 127) // 128) * batch / (2.0 * sms)
 
 
-def classify(M: int, N: int, aligned: bool, batch: int = 1) -> str:
-    """The class of a problem (mirrors table_choose in config_table.h)."""
+def classify(M: int, N: int, aligned: bool, batch: int = 1, sms: int = SMS) -> str:
+    """The class of a problem on a part with `sms` multiprocessors (mirrors table_choose in
+    config_table.h)."""
     prefix = "aligned" if aligned else "unaligned"
     if M * N * batch <= 512 * 512:
         return prefix + "_tiny"
-    w = waves(M, N, batch)
+    w = waves(M, N, batch, sms)
     if w < 1.0:
         return prefix + "_small"
     if w < 6.0:

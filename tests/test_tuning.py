@@ -43,3 +43,40 @@ def test_library_follows_the_class_table(sgemm_lib):
                                               (1000, 1000, False, "unaligned_small")])
 def test_classify(M, N, aligned, want):
     assert classes.classify(M, N, aligned) == want
+
+
+def test_classify_follows_the_sm_count():
+    # 4096 x 4096 is 1024 tiles of 128 x 128: 3.4 waves at two CTAs per SM on 152 SMs,
+    # 6.7 waves on a 76-SM part (one die), so the same shape changes class.
+    assert classes.classify(4096, 4096, True, sms=152) == "aligned_medium"
+    assert classes.classify(4096, 4096, True, sms=76) == "aligned_large"
+    assert classes.classify(1024, 1024, True, sms=152) == "aligned_small"
+    assert classes.classify(1024, 1024, True, sms=16) == "aligned_medium"
+
+
+def test_library_class_rule_follows_the_sm_count(tmp_path):
+    # The header's rule, compiled on the host, classifies the same shape by the SM count it is
+    # given (the library passes the current device's multiprocessor count).
+    import shutil
+    import subprocess
+    from pathlib import Path
+    root = Path(__file__).resolve().parents[1]
+    csrc = root / "dense_fp32_gemm_08_gb300" / "csrc"
+    cuda_inc = Path("/usr/local/cuda/include")
+    if not (cuda_inc / "cuda_runtime.h").exists() or shutil.which("g++") is None:
+        pytest.skip("needs g++ and the CUDA headers")
+    src = tmp_path / "cls.cpp"
+    src.write_text(
+        '#include "config_table.h"\n#include <cstdio>\n'
+        "int main() {\n"
+        "  sg::SimtProblem p{};\n"
+        "  p.M = 4096; p.N = 4096; p.K = 4096; p.batch = 1;\n"
+        "  std::printf(\"%d %d %d\\n\", sg::shape_class(p, true, 152), sg::shape_class(p, true, 76),"
+        " sg::shape_class(p, true, 0));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "cls"
+    subprocess.run(["g++", "-std=c++17", f"-I{csrc}", f"-I{cuda_inc}", str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    order = classes.CLASS_ORDER
+    assert [order[int(x)] for x in out] == ["aligned_medium", "aligned_large", "aligned_medium"]
