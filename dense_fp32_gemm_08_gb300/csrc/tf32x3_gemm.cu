@@ -7,7 +7,8 @@
 // small.big misses only small.small (about 2^-22 relative) and the rounding of small. A
 // pre-pass writes A's parts row-major (K contiguous) and B's parts transposed (N x K, K
 // contiguous), so both MMA operands are K-major in shared memory. Non-finite values keep
-// big = x and small = 0, so Inf and NaN propagate as in fp32.
+// big = x and small = 0, so Inf and NaN propagate as in fp32; finite values whose rounding
+// would overflow (within half a TF32 step of FLT_MAX) are truncated instead.
 //
 // GEMM. A persistent grid (one CTA per SM) walks the 128 x BN output tiles in grouped-raster
 // order, tile t, t + grid, ...; 6 warps per CTA:
@@ -62,9 +63,19 @@ __device__ __forceinline__ float tf32_rna(float x) {
     return __uint_as_float(r);
 }
 
+// x = big + small. A finite x within half a TF32 step of FLT_MAX rounds up past the largest
+// exponent; for those, big keeps x's top bits (truncation) so that big stays finite and
+// small = x - big is exact. Non-finite x: big = x, small = 0.
 __device__ __forceinline__ void split_value(float x, float &big, float &small) {
     big = tf32_rna(x);
-    small = isfinite(big) ? tf32_rna(x - big) : 0.0f;
+    if (isfinite(big)) {
+        small = tf32_rna(x - big);
+    } else if (isfinite(x)) {
+        big = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+        small = tf32_rna(x - big);
+    } else {
+        small = 0.0f;
+    }
 }
 
 // A (rows x cols, leading dimension lda, batch stride sA) -> big, small (rows x ldo each,

@@ -111,3 +111,29 @@ def test_strided_batched(sg):
         den = oracle.absdot(M, N, K, a, K, bb, N)
         got = out[b * sC:b * sC + M * N].reshape(M, N)
         assert oracle.normalized_error(got, ref, den, 0.7, -1.3, c.reshape(M, N)) <= TOL
+
+
+@pytest.mark.parametrize("entry,bound", [("sgemm_3xtf32", TOL), ("sgemm_tf32", 1e-3)])
+def test_values_near_flt_max_stay_finite(sg, entry, bound):
+    # FLT_MAX rounds to Inf under round-to-nearest-away to TF32; the split must keep such a
+    # value finite, so the product matches fp32 arithmetic (and the oracle) instead of
+    # overflowing. A's first row holds +-FLT_MAX in two places, B's matching rows hold 1/8,
+    # so the result stays far from the fp32 limit.
+    import oracle
+    import synth
+    M, N, K = 64, 96, 80
+    fmax = float(np.finfo(np.float32).max)
+    A = synth.normal(M, K, 70)
+    B = synth.normal(K, N, 71)
+    A[0, 3], A[5, 40] = fmax, -fmax
+    B[3, :] = 0.125
+    B[40, :] = 0.125
+    C = np.zeros((M, N), np.float32)
+    dA, dB, dC = (torch.from_numpy(x.copy()).cuda() for x in (A, B, C))
+    getattr(sg, entry)(M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N)
+    assert sg.sgemm_device_status() == sg.SGEMM_OK
+    got = dC.cpu().numpy()
+    assert np.isfinite(got).all(), f"{entry}: non-finite result from finite inputs"
+    ref = oracle.sgemm(M, N, K, 1.0, A, K, B, N, 0.0, None, N)
+    den = oracle.absdot(M, N, K, A, K, B, N)
+    assert oracle.normalized_error(got, ref, den, 1.0, 0.0, None) <= bound
