@@ -252,11 +252,20 @@ def _batched(sg, M, N, K, batch, sA, sB, sC, alpha, beta, entry, exact=False):
     del g
 
 
+def _config_id(sg, name):
+    """Configuration id by name (None: the per-shape table's choice)."""
+    if name is None:
+        return -1
+    ids = {sg.sgemm_config_name(i): i for i in range(sg.sgemm_num_configs())}
+    return ids[name]
+
+
 @pytest.mark.parametrize("M,N,K,batch", [(128, 256, 64, 3), (65, 33, 17, 5), (256, 256, 256, 2),
                                          (512, 768, 300, 7)])
-@pytest.mark.parametrize("cfg", [-1, 5, 6, 8])
+@pytest.mark.parametrize("cfg", [None, "sk_tma_ws_128x256_s4", "pdp_tma_ws_128x256_s4",
+                                 "sk_tma_ws_128x128_s3"])
 def test_strided_batched(sg, M, N, K, batch, cfg):
-    sg.sgemm_force_config(cfg)
+    sg.sgemm_force_config(_config_id(sg, cfg))
     try:
         _batched(sg, M, N, K, batch, M * K, K * N, M * N, 0.7, -1.3, sg.sgemm_strided_batched)
         _batched(sg, M, N, K, batch, M * K, K * N, M * N, 1.0, 1.0, sg.sgemm_strided_batched,
@@ -265,10 +274,11 @@ def test_strided_batched(sg, M, N, K, batch, cfg):
         sg.sgemm_force_config(-1)
 
 
-@pytest.mark.parametrize("cfg", [-1, 14, 15, 18])
+@pytest.mark.parametrize("cfg", [None, "packed_sk_tma_128x256_s4", "packed_dp_tma_128x128_s3",
+                                 "packed_sk_tma_256x128_k64_s2"])
 def test_strided_batched_unaligned(sg, cfg):
     # odd leading dimensions and strides: repacked for TMA (or loaded with cp.async)
-    sg.sgemm_force_config(cfg)
+    sg.sgemm_force_config(_config_id(sg, cfg))
     try:
         M, N, K, batch = 129, 131, 75, 3
         import oracle

@@ -1,8 +1,10 @@
 """sgemm_noalloc: the entry point for callers that must not have the library allocate device
 memory (their memory budget belongs to their own pool, or they cannot take the
 synchronisation that cudaMalloc / cudaFree may cause). Its scratch is a static array in the
-library. Through the C ABI, two calls in a row must each agree with sgemm() on the same
-inputs, within the normalised-error bound every GPU test here uses.
+library. Through the C ABI, two calls in a row must each agree with the oracle (on a sample
+of rows) and with sgemm() (on the whole matrix) on the same inputs, within the
+normalised-error bound every GPU test here uses, and must leave the device's free memory
+unchanged.
 
 This file is collected last on purpose: if it fails, every other test has already run."""
 from __future__ import annotations
@@ -45,19 +47,35 @@ def test_noalloc_matches_sgemm_twice(sgemm_lib, M, N, K, alpha, beta):
     assert L.sgemm_device_status(stream) == 0
     ref_h = ref.cpu().numpy()
 
-    rows = np.unique(np.r_[0, M - 1, np.linspace(0, M - 1, 24).astype(int)])
+    # The oracle on a sample of rows: first, last, the last row tile and an even spread.
+    rows = np.unique(np.r_[0, M - 1, np.arange(max(0, M - 128), M, 37),
+                          np.linspace(0, M - 1, 24).astype(int)])
+    want = oracle.sgemm(M, N, K, alpha, A, K, B, N, beta, C, N, rows=rows)
     den = oracle.absdot(M, N, K, A, K, B, N, rows=rows)
+
+    # Every buffer exists before the calls under test; one warm-up call does the per-device
+    # set-up (the array's address, kernel attributes, the module's first load).
+    outs = [_to_dev(C) for _ in range(3)]
+    st = L.sgemm_noalloc(M, N, K, ctypes.c_float(alpha), dA.data_ptr(), K, dB.data_ptr(), N,
+                         ctypes.c_float(beta), outs[2].data_ptr(), N, stream)
+    assert st == 0, f"warm-up call: {L.sgemm_last_error()}"
+    assert L.sgemm_device_status(stream) == 0
+    free_before = torch.cuda.mem_get_info()[0]
     for call in range(2):
-        out = _to_dev(C)
         st = L.sgemm_noalloc(M, N, K, ctypes.c_float(alpha), dA.data_ptr(), K, dB.data_ptr(), N,
-                             ctypes.c_float(beta), out.data_ptr(), N, stream)
+                             ctypes.c_float(beta), outs[call].data_ptr(), N, stream)
         assert st == 0, f"call {call}: {L.sgemm_last_error()}"
         assert L.sgemm_device_status(stream) == 0, f"call {call}: device status"
-        got = out.cpu().numpy()
-        # the whole matrix against sgemm(), scaled by the rows' magnitudes
+    free_after = torch.cuda.mem_get_info()[0]
+    assert free_after == free_before, "device memory changed across the no-allocation calls"
+
+    for call in range(2):
+        got = outs[call].cpu().numpy()
         assert np.isfinite(got).all()
-        err = oracle.normalized_error(got[rows], ref_h[rows], den, alpha, beta, C[rows])
-        assert err <= TOL, f"call {call}: normalised difference {err:.3e}"
+        # against the oracle, within the bound every GPU test here uses
+        err = oracle.normalized_error(got[rows], want, den, alpha, beta, C[rows])
+        assert err <= TOL, f"call {call}: normalised error {err:.3e} against the oracle"
+        # and against sgemm(), the entry point it stands in for, on the whole matrix
         scale = np.abs(A).sum(axis=1, keepdims=True) * np.abs(B).max() + abs(beta) * np.abs(C)
         assert (np.abs(got - ref_h) <= TOL * scale).all(), f"call {call}: differs from sgemm()"
 
