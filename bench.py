@@ -5,14 +5,26 @@ beta = 0 (the pages' headline problem, 137.4 GFLOP per call). A "step" is one li
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload headline|sq256|edge0..edge3|sweepNNNN|llm_qkv|llm_up|llm_down|llm_head]
-                  [--path simt|3xtf32|tf32]
+                  [--path simt|3xtf32|tf32] [--no-paths] [--no-sweep]
 
-Timing: W untimed warm-up steps, then K steps. Before every step a 256 MiB buffer is written
-(L2 is 129 MB) so each step starts with cold L2; each step's GEMM is bracketed by CUDA
+Timing: W untimed warm-up steps, then exactly K steps. Before every step a 256 MiB buffer is
+written (L2 is 129 MB) so each step starts with cold L2; each step's GEMM is bracketed by CUDA
 events on the stream it runs on. value = 2*M*N*K * K_steps * ranks / max over ranks of the
-summed GEMM time. Under torchrun (N > 1) every rank runs its own replica of the workload
-(the method shards without communication; no collective is on the data path) and the max
-of the per-rank times is taken through the process group.
+summed GEMM time. SM clocks and clock-event reasons are sampled in process through NVML every
+2 ms during the timed steps (nvidia-smi every 20 ms as well); a `sustained` block then repeats
+the step for at least one second under the same sampling. Under torchrun (N > 1) every rank
+runs its own replica of the workload (the method shards without communication; no collective
+is on the data path) and the max of the per-rank times is taken through the process group.
+
+After the headline line's own measurement (and outside its timed region) the same run reports
+`paths` (the 3xTF32 and TF32 tensor-core paths on the same workload, against the TF32 peak)
+and `sweep` (the square sizes 128..16384, the four edge shapes and the four LLM-layer shapes
+on the SIMT path, each with cuBLAS SGEMM timed beside it under the same rules). Sweep inputs
+are drawn on the device from torch's seeded generator with the workloads' distributions.
+
+The CPU baseline times the oracle on a row sample of the workload; the same rows of the
+timed call's result are compared with the oracle's (the `check` block) and the run fails
+if they exceed the 1e-5 normalised bound.
 
 The reference arm (--impl reference) times the CPU oracle (fp64 triple loop, all host cores)
 on a bounded row sample of the same workload, each step one sample.
@@ -173,6 +185,89 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz)}
 
 
+class NvmlClocks:
+    """Samples the SM clock and the clock-event reasons in process through NVML (ctypes on the
+    driver's libnvidia-ml), every `period_s` seconds, while a region runs. The GPU is found by
+    its UUID (falling back to the NVML index), so CUDA_VISIBLE_DEVICES renumbering is harmless.
+    Reading clocks changes no setting."""
+
+    _CLOCK_SM = 1
+
+    def __init__(self, uuid: str | None, index: int, period_s: float = 0.002):
+        self.uuid, self.index, self.period_s = uuid, index, period_s
+        self.samples: list[tuple[float, int]] = []
+        self.max_mhz = None
+        self._lib = self._handle = self._thread = None
+        self._stop = threading.Event()
+
+    def _open(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        handle = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(handle)) == 0
+        if not ok:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(handle)) == 0
+        if not ok:
+            return False
+        self._reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(handle, self._CLOCK_SM, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self._lib, self._handle = lib, handle
+        return True
+
+    def _run(self):
+        import ctypes
+        mhz, bits = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if (self._lib.nvmlDeviceGetClockInfo(self._handle, self._CLOCK_SM, ctypes.byref(mhz)) == 0
+                    and self._reasons(self._handle, ctypes.byref(bits)) == 0):
+                self.samples.append((float(mhz.value), int(bits.value)))
+            self._stop.wait(self.period_s)
+
+    def __enter__(self):
+        try:
+            if self._open():
+                self._thread = threading.Thread(target=self._run, daemon=True)
+                self._thread.start()
+        except (OSError, AttributeError):
+            self._lib = None
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        reasons = sorted({name for _, b in self.samples for bit, name in _REASON_BITS.items()
+                          if b & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples),
+                "sm_max_mhz": self.max_mhz or max(m for m, _ in self.samples),
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def merge_clocks(nvml: dict, smi: dict) -> dict:
+    """The clock record of a region: NVML's in-process samples when there are any, else
+    nvidia-smi's; reasons are the union of both."""
+    base = nvml if nvml.get("samples") else smi
+    out = {"sm_mhz": base.get("sm_mhz"), "sm_max_mhz": base.get("sm_max_mhz") or smi.get("sm_max_mhz"),
+           "reasons": sorted(set(nvml.get("reasons", [])) | set(smi.get("reasons", []))),
+           "samples": base.get("samples", 0), "source": "nvml" if base is nvml else "nvidia-smi",
+           "smi_samples": smi.get("samples", 0)}
+    return out
+
+
 # ---- profiles (ncu traffic figures committed under profiles/) --------------------------------------
 
 KERNEL_SOURCES = {
@@ -222,7 +317,8 @@ def measured_peaks():
 # ---- CPU oracle baseline -------------------------------------------------------------------------
 
 class OracleTimer:
-    """Times the CPU oracle on seeded row samples of a workload (all N columns, full K)."""
+    """Times the CPU oracle on seeded row samples of a workload (all N columns, full K). The
+    last sample's row indices and result rows are kept (`last_rows`, `last_out`)."""
 
     def __init__(self, w, A, B, C):
         import numpy as np
@@ -233,6 +329,7 @@ class OracleTimer:
         self.rng = np.random.default_rng(0)
         self.np = np
         self.per_row = None
+        self.last_rows = self.last_out = None
 
     def run(self, nrows: int) -> tuple[float, int]:
         w = self.w
@@ -240,9 +337,11 @@ class OracleTimer:
         rows = self.np.sort(self.rng.choice(M, size=min(nrows, M), replace=False))
         beta = w["beta"]
         t0 = time.perf_counter()
-        self.oracle.sgemm(M, N, K, w["alpha"], self.A, K, self.B, N, beta,
-                          self.C if beta != 0.0 else None, N, rows=rows)
-        return time.perf_counter() - t0, len(rows)
+        out = self.oracle.sgemm(M, N, K, w["alpha"], self.A, K, self.B, N, beta,
+                                self.C if beta != 0.0 else None, N, rows=rows)
+        dt = time.perf_counter() - t0
+        self.last_rows, self.last_out = rows, out
+        return dt, len(rows)
 
     def rows_for(self, seconds: float) -> int:
         if self.per_row is None:
@@ -252,9 +351,30 @@ class OracleTimer:
         return int(min(self.w["M"], max(1, seconds / self.per_row)))
 
 
-def oracle_sample(w, target_s: float, A, B, C, threads: int | None = None):
+CHECK_BOUND = 1e-5
+CHECK_ROWS = 64
+
+
+def result_check(w, A, B, C, rows, want, got_full):
+    """Normalised error of the GPU result rows against the oracle rows just timed (at most
+    CHECK_ROWS of them, spread over the sample)."""
+    import numpy as np
+    import oracle
+    M, N, K = w["M"], w["N"], w["K"]
+    pick = np.unique(np.linspace(0, len(rows) - 1, min(CHECK_ROWS, len(rows))).astype(int))
+    r = rows[pick]
+    den = oracle.absdot(M, N, K, A, K, B, N, rows=r)
+    err = oracle.normalized_error(got_full[r], want[pick], den, w["alpha"], w["beta"],
+                                  C[r] if w["beta"] != 0.0 else None)
+    return {"rows": int(len(r)), "normalized_error": float(err), "bound": CHECK_BOUND,
+            "ok": bool(err <= CHECK_BOUND),
+            "what": "result of the timed call against the oracle rows of the cpu_baseline sample"}
+
+
+def oracle_sample(w, target_s: float, A, B, C, threads: int | None = None, result=None):
     """Times the oracle on a row sample sized for about `target_s` seconds, on `threads`
-    OpenMP threads (default: all). Returns (gflops, seconds, rows, threads)."""
+    OpenMP threads (default: all). Returns (gflops, seconds, rows, threads, check), where
+    check compares `result` (the GPU's C, when given) with the sampled oracle rows."""
     import oracle
     full = oracle.max_threads()
     if threads is not None:
@@ -266,10 +386,73 @@ def oracle_sample(w, target_s: float, A, B, C, threads: int | None = None):
         dt, n = t.run(t.rows_for(target_s))
     finally:
         oracle.set_threads(full)
-    return 2.0 * n * w["N"] * w["K"] / dt / 1e9, dt, n, t.threads
+    check = None
+    if result is not None:
+        check = result_check(w, A, B, C, t.last_rows, t.last_out, result)
+    return 2.0 * n * w["N"] * w["K"] / dt / 1e9, dt, n, t.threads, check
 
 
-# ---- our arm ---------------------------------------------------------------------------------------
+def device_inputs(torch, dev, w, seed=0):
+    """Sweep inputs drawn on the device from torch's seeded generator with the workload's
+    distribution (uniform [-1, 1), N(0, 1), or the LLM recipe with B ~ N(0, 0.02^2))."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    M, N, K = w["M"], w["N"], w["K"]
+
+    def draw(rows, cols, kind, sigma=1.0):
+        if kind == "uniform":
+            return torch.rand(rows, cols, generator=g, device=dev) * 2.0 - 1.0
+        return torch.randn(rows, cols, generator=g, device=dev) * sigma
+
+    if w["dist"] == "llm":
+        return draw(M, K, "normal"), draw(K, N, "normal", 0.02), draw(M, N, "normal")
+    return draw(M, K, w["dist"]), draw(K, N, w["dist"]), draw(M, N, w["dist"])
+
+
+def time_steps(torch, stream, step, n, flush, restore=None):
+    """Runs `step` n times, each after an L2 flush (and `restore`, e.g. C <- C0), and returns
+    each call's device time in ms (CUDA events on `stream` around the call only)."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        flush.fill_(float(i))
+        if restore is not None:
+            restore()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def simt_peak_tflops(sms, mhz=BOOST_MHZ):
+    return sms * mhz * 1e6 * FMA_PER_CLK_PER_SM * 2 / 1e12
+
+
+def tf32_peak():
+    """(TF32 dense peak in TFLOP/s, basis): the measured bf16 burst peak scaled by the nominal
+    TF32:BF16 ratio, else the nominal TF32 rate."""
+    peaks = measured_peaks()
+    if peaks.get("bf16_tflops"):
+        return (peaks["bf16_tflops"] * TF32_NOMINAL_TFLOPS / BF16_NOMINAL_TFLOPS,
+                f"measured bf16 {peaks['bf16_tflops']} TFLOP/s x nominal TF32:BF16 "
+                f"{TF32_NOMINAL_TFLOPS:g}:{BF16_NOMINAL_TFLOPS:g} (of measured)")
+    return TF32_NOMINAL_TFLOPS, "nominal dense TF32 rate (no measured peak file: of fallback)"
+
+
+def tensor_roofline(path, achieved_tflops, workload, sms):
+    products = 3 if path == "3xtf32" else 1
+    peak, basis = tf32_peak()
+    kernel = {"3xtf32": "tf32x3_tcgen05", "tf32": "tf32_tcgen05"}[path]
+    return {"bound": "tensor", "achieved": round(achieved_tflops, 3), "peak": round(peak, 1),
+            "unit": "TFLOP/s", "frac": round(achieved_tflops / peak, 4),
+            "issued_tflops": round(products * achieved_tflops, 3),
+            "issued_frac": round(products * achieved_tflops / peak, 4),
+            "traffic": ncu_traffic(kernel, workload, "3xtf32"),
+            "peak_basis": basis + f"; achieved counts 2MNK, issued counts the {products} "
+                                  "TF32 product(s) per multiply-add",
+            "frac_of_fp32_simt_peak": round(achieved_tflops / simt_peak_tflops(sms), 4)}
+
 
 def run_ours(args):
     import torch
@@ -282,7 +465,8 @@ def run_ours(args):
     w = WORKLOADS[args.workload]
     M, N, K, alpha, beta = w["M"], w["N"], w["K"], w["alpha"], w["beta"]
     flops = 2.0 * M * N * K
-    entry = {"simt": sg.sgemm, "3xtf32": sg.sgemm_3xtf32, "tf32": sg.sgemm_tf32}[args.path]
+    entries = {"simt": sg.sgemm, "3xtf32": sg.sgemm_3xtf32, "tf32": sg.sgemm_tf32}
+    entry = entries[args.path]
 
     A_h, B_h, C_h = host_inputs(w)
     A = torch.from_numpy(A_h).to(dev)
@@ -294,45 +478,52 @@ def run_ours(args):
     cfg_id = sg.sgemm_select_config(M, N, K, alpha, A, K, B, N, C, N)
     kernel = (sg.sgemm_config_name(cfg_id) if args.path == "simt"
               else {"3xtf32": "tf32x3_tcgen05", "tf32": "tf32_tcgen05"}[args.path])
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    uuid = getattr(props, "uuid", None)
+    uuid = f"GPU-{uuid}" if uuid and not str(uuid).startswith("GPU-") else (str(uuid) if uuid else None)
+    restore = (lambda: C.copy_(C0)) if C0 is not None else None
 
     def step():
         entry(M, N, K, alpha, A, K, B, N, beta, C, N, stream)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        if C0 is not None:
-            C.copy_(C0)
+        if restore:
+            restore()
         step()
     torch.cuda.synchronize(dev)
     if sg.sgemm_device_status(stream) != sg.SGEMM_OK:
         raise RuntimeError(f"device status after warm-up: {sg.sgemm_last_error()}")
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # ---- the timed region: exactly `steps` calls ----
     barrier(dist)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clocks:
+    with ClockSampler(local, period_ms=20) as smi, NvmlClocks(uuid, local) as nv:
         wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.fill_(float(i))
-            if C0 is not None:   # beta != 0: restore C so every step computes the same thing
-                C.copy_(C0)
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
+        step_ms = time_steps(torch, stream, step, args.steps, flush, restore)
         wall = time.perf_counter() - wall0
     barrier(dist)
     if sg.sgemm_device_status(stream) != sg.SGEMM_OK:
         raise RuntimeError(f"device status after timing: {sg.sgemm_last_error()}")
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    result_host = C.cpu().numpy() if rank == 0 and not args.no_cpu_baseline else None
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
     value = flops * args.steps * world / (total_ms / 1e3) / 1e9
+    clk = merge_clocks(nv.summary(), smi.summary())
 
-    props = torch.cuda.get_device_properties(dev)
-    sms = props.multi_processor_count
-    clk = clocks.summary()
-    peak_boost = sms * BOOST_MHZ * 1e6 * FMA_PER_CLK_PER_SM * 2 / 1e12   # TFLOP/s
+    # ---- the same step for at least a second: the clock the kernel sustains ----
+    sustained = None
+    if not args.no_sustained:
+        with ClockSampler(local, period_ms=20) as smi2, NvmlClocks(uuid, local, 0.01) as nv2:
+            t0, ms_all = time.perf_counter(), []
+            while time.perf_counter() - t0 < args.sustain_s:
+                ms_all += time_steps(torch, stream, step, args.steps, flush, restore)
+        c2 = merge_clocks(nv2.summary(), smi2.summary())
+        sustained = {"steps": len(ms_all), "seconds": round(time.perf_counter() - t0, 3),
+                     "value": round(flops * len(ms_all) / (sum(ms_all) / 1e3) / 1e9, 1),
+                     "unit": UNIT, "clocks": c2}
+
+    peak_boost = simt_peak_tflops(sms)
     avg_ms = sum(step_ms) / len(step_ms)
     achieved_tflops = flops / (avg_ms / 1e3) / 1e12
     if args.path == "simt":
@@ -341,27 +532,10 @@ def run_ours(args):
                 "traffic": ncu_traffic(kernel, args.workload, "simt"),
                 "peak_basis": f"{sms} SMs x {BOOST_MHZ:.0f} MHz x {FMA_PER_CLK_PER_SM} FMA/clk x 2"}
         if clk.get("sm_mhz"):
-            roof["frac_at_run_clock"] = round(
-                achieved_tflops / (sms * clk["sm_mhz"] * 1e6 * FMA_PER_CLK_PER_SM * 2 / 1e12), 4)
+            roof["frac_at_run_clock"] = round(achieved_tflops / simt_peak_tflops(sms, clk["sm_mhz"]), 4)
+            roof["run_clock_basis"] = f"median of {clk['samples']} {clk['source']} samples"
     else:
-        products = 3 if args.path == "3xtf32" else 1
-        peaks = measured_peaks()
-        if peaks.get("bf16_tflops"):
-            tf32_peak = peaks["bf16_tflops"] * TF32_NOMINAL_TFLOPS / BF16_NOMINAL_TFLOPS
-            basis = (f"measured bf16 {peaks['bf16_tflops']} TFLOP/s x nominal TF32:BF16 "
-                     f"{TF32_NOMINAL_TFLOPS:g}:{BF16_NOMINAL_TFLOPS:g}")
-        else:
-            tf32_peak = TF32_NOMINAL_TFLOPS
-            basis = "nominal dense TF32 rate (no measured peak file)"
-        roof = {"bound": "tensor", "achieved": round(achieved_tflops, 3),
-                "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved_tflops / tf32_peak, 4),
-                "issued_tflops": round(products * achieved_tflops, 3),
-                "issued_frac": round(products * achieved_tflops / tf32_peak, 4),
-                "traffic": ncu_traffic(kernel, args.workload, "3xtf32"),
-                "peak_basis": basis + f"; achieved counts 2MNK, issued counts the {products} "
-                                      "TF32 product(s) per multiply-add",
-                "frac_of_fp32_simt_peak": round(achieved_tflops / peak_boost, 4)}
+        roof = tensor_roofline(args.path, achieved_tflops, args.workload, sms)
 
     e2e = None
     if not args.no_e2e:
@@ -383,29 +557,116 @@ def run_ours(args):
         "roofline": roof,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "clock_samples": clk["samples"],
+        "clock_source": clk["source"],
+        "clock_samples_smi": clk["smi_samples"],
+        "sustained": sustained,
         "gpu_launches": args.steps * launches_per_call(args.path, kernel, w),
         "wall_s_timed_loop": round(wall, 4),
         "e2e": e2e,
         "device": props.name, "sms": sms,
     }
     if rank == 0 and not args.no_cublas_context:
-        line["context_cublas"] = cublas_context(torch, dev, stream, w, A, B, C, C0, flush,
-                                                max(3, args.warmup), min(args.steps, 50),
+        line["context_cublas"] = cublas_context(torch, stream, w, A, B, C0 if C0 is not None else C,
+                                                flush, max(3, args.warmup), min(args.steps, 50),
                                                 value / world)
+    if rank == 0 and args.path == "simt" and not args.no_paths:
+        line["paths"] = measure_paths(args, torch, sg, stream, w, A, B, C, restore, flush, sms)
+    if rank == 0 and not args.no_sweep:
+        del A, B, C, C0
+        torch.cuda.empty_cache()
+        line["sweep"] = measure_sweep(torch, sg, dev, stream, flush, sms, args.sweep_steps)
     if rank == 0 and not args.no_cpu_baseline:
-        gf, dt, nrows, threads = oracle_sample(w, args.cpu_seconds, A_h, B_h, C_h)
+        gf, dt, nrows, threads, check = oracle_sample(w, args.cpu_seconds, A_h, B_h, C_h,
+                                                      result=result_host)
         line["cpu_baseline"] = {"value": round(gf, 3), "unit": UNIT, "cores": threads,
                                 "kind": "oracle",
                                 "sample": f"{nrows} of {M} result rows (all N columns, full K), "
                                           f"{dt:.1f} s, fp64 triple loop, OpenMP over rows"}
-        gf1, dt1, n1, _ = oracle_sample(w, args.cpu_seconds / 4, A_h, B_h, C_h, threads=1)
+        gf1, dt1, n1, _, _ = oracle_sample(w, args.cpu_seconds / 4, A_h, B_h, C_h, threads=1)
         line["cpu_baseline"]["single_core"] = {
             "value": round(gf1, 3), "unit": UNIT, "cores": 1,
             "sample": f"{n1} of {M} result rows (all N columns, full K), {dt1:.1f} s"}
+        line["check"] = check
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+    if rank == 0 and line.get("check") and not line["check"]["ok"]:
+        raise SystemExit(f"the timed result differs from the oracle: {line['check']}")
+
+
+def measure_paths(args, torch, sg, stream, w, A, B, C, restore, flush, sms):
+    """The tensor-core paths on the bench's workload, under the same timing rules."""
+    M, N, K, alpha, beta = w["M"], w["N"], w["K"], w["alpha"], w["beta"]
+    flops = 2.0 * M * N * K
+    out = {}
+    for path, entry in (("3xtf32", sg.sgemm_3xtf32), ("tf32", sg.sgemm_tf32)):
+        def step(entry=entry):
+            entry(M, N, K, alpha, A, K, B, N, beta, C, N, stream)
+        for _ in range(3):
+            flush.fill_(1.0)
+            if restore:
+                restore()
+            step()
+        ms = time_steps(torch, stream, step, max(3, min(args.steps, 20)), flush, restore)
+        if sg.sgemm_device_status(stream) != sg.SGEMM_OK:
+            raise RuntimeError(f"device status after the {path} path: {sg.sgemm_last_error()}")
+        avg = sum(ms) / len(ms)
+        tflops = flops / (avg / 1e3) / 1e12
+        kernel = {"3xtf32": "tf32x3_tcgen05", "tf32": "tf32_tcgen05"}[path]
+        out[path] = {"value": round(tflops * 1e3, 1), "unit": UNIT, "ms_per_step": round(avg, 4),
+                     "steps": len(ms), "kernel": kernel,
+                     "gpu_launches_per_call": launches_per_call(path, kernel, w),
+                     "roofline": tensor_roofline(path, tflops, args.workload, sms)}
+    return out
+
+
+SWEEP = ([f"sweep{n}" for n in (128, 256, 512, 1024, 2048, 4096, 8192, 16384)] +
+         ["edge0", "edge1", "edge2", "edge3", "llm_qkv", "llm_up", "llm_down", "llm_head"])
+
+
+def measure_sweep(torch, sg, dev, stream, flush, sms, steps):
+    """GFLOP/s of the SIMT path (and of cuBLAS SGEMM, TF32 off, beside it) on every sweep,
+    edge and LLM workload: a few steps each, L2 flushed before every call, CUDA events."""
+    peak = simt_peak_tflops(sms)
+    rows = []
+    for name in SWEEP:
+        w = WORKLOADS[name]
+        M, N, K, alpha, beta = w["M"], w["N"], w["K"], w["alpha"], w["beta"]
+        flops = 2.0 * M * N * K
+        A, B, C = device_inputs(torch, dev, w)
+        C0 = C.clone() if beta != 0.0 else None
+        restore = (lambda: C.copy_(C0)) if C0 is not None else None
+        cfg = sg.sgemm_config_name(sg.sgemm_select_config(M, N, K, alpha, A, K, B, N, C, N))
+
+        def step():
+            sg.sgemm(M, N, K, alpha, A, K, B, N, beta, C, N, stream)
+        for _ in range(2):
+            flush.fill_(1.0)
+            step()
+        n = steps if flops < 2e12 else max(3, steps // 2)
+        ms = time_steps(torch, stream, step, n, flush, restore)
+        if sg.sgemm_device_status(stream) != sg.SGEMM_OK:
+            raise RuntimeError(f"device status after sweep {name}: {sg.sgemm_last_error()}")
+        avg = sum(ms) / len(ms)
+        gf = flops / (avg / 1e3) / 1e9
+        cub = cublas_context(torch, stream, w, A, B, C0 if C0 is not None else C, flush, 2, n, gf)
+        row = {"workload": workload_name(name, w), "config": cfg, "gflops": round(gf, 1),
+               "ms": round(avg, 4), "steps": n,
+               "pct_fp32_simt_peak": round(100.0 * gf / (peak * 1e3), 2),
+               "cublas_gflops": cub["value"], "ours_over_cublas": cub["ours_over_it"]}
+        if min(M, N) <= 8:   # HBM-bound: the bytes of the large operand and of C
+            nbytes = 4 * (M * K + K * N + M * N * (2 if beta != 0.0 else 1))
+            row["gbs"] = round(nbytes / (avg / 1e3) / 1e9, 1)
+            hbm = measured_peaks().get("hbm_gbs")
+            if hbm:
+                row["pct_hbm_measured"] = round(100.0 * row["gbs"] / hbm, 2)
+        rows.append(row)
+        del A, B, C, C0
+        torch.cuda.empty_cache()
+    return {"path": "simt", "inputs": "device-drawn from torch's seeded generator (seed 0), "
+                                      "the workloads' distributions",
+            "l2": "flushed before every call (256 MiB write)", "rows": rows}
 
 
 def launches_per_call(path: str, kernel: str, w) -> int:
@@ -421,32 +682,26 @@ def launches_per_call(path: str, kernel: str, w) -> int:
     return n
 
 
-def cublas_context(torch, dev, stream, w, A, B, C, C0, flush, warmup, steps, ours):
+def cublas_context(torch, stream, w, A, B, Csrc, flush, warmup, steps, ours):
     """The same workload through torch.addmm (cuBLAS SGEMM, TF32 off) under the same timing
-    rules: a comparison bar only, never a path of the library."""
+    rules (out = alpha * A.B + beta * Csrc into a separate buffer): a comparison bar only,
+    never a path of the library."""
     M, N, K, alpha, beta = w["M"], w["N"], w["K"], w["alpha"], w["beta"]
     flops = 2.0 * M * N * K
     prev = torch.backends.cuda.matmul.allow_tf32
     torch.backends.cuda.matmul.allow_tf32 = False
-    out = torch.empty_like(C)
-    src = C0 if C0 is not None else C
+    out = torch.empty_like(Csrc)
     try:
         with torch.cuda.stream(stream):
             for _ in range(warmup):
                 flush.fill_(1.0)
-                torch.addmm(src, A, B, beta=beta, alpha=alpha, out=out)
-            ms = []
-            for i in range(steps):
-                flush.fill_(float(i))
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                torch.addmm(src, A, B, beta=beta, alpha=alpha, out=out)
-                e1.record(stream)
-                e1.synchronize()
-                ms.append(e0.elapsed_time(e1))
+                torch.addmm(Csrc, A, B, beta=beta, alpha=alpha, out=out)
+            ms = time_steps(torch, stream,
+                            lambda: torch.addmm(Csrc, A, B, beta=beta, alpha=alpha, out=out),
+                            steps, flush)
     finally:
         torch.backends.cuda.matmul.allow_tf32 = prev
+    del out
     gf = flops * len(ms) / (sum(ms) / 1e3) / 1e9
     return {"value": round(gf, 1), "unit": UNIT, "library": "torch.addmm (cuBLAS SGEMM), TF32 off",
             "steps": len(ms), "ours_over_it": round(ours / gf, 3)}
@@ -551,6 +806,14 @@ def parse(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="headline")
     ap.add_argument("--path", choices=["simt", "3xtf32", "tf32"], default="simt")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-paths", action="store_true",
+                    help="skip the 3xTF32 / TF32 tensor-core paths on the workload")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the size / edge / LLM-shape sweep of the SIMT path")
+    ap.add_argument("--sweep-steps", type=int, default=6, help="timed calls per sweep workload")
+    ap.add_argument("--no-sustained", action="store_true",
+                    help="skip the one-second sustained loop after the timed steps")
+    ap.add_argument("--sustain-s", type=float, default=1.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cublas-context", action="store_true",

@@ -123,9 +123,40 @@ def test_oracle_sample_single_core_restores_threads():
     full = oracle.max_threads()
     w = bench.WORKLOADS["sq256"]
     A, B, C = bench.host_inputs(w)
-    gf, dt, n, threads = bench.oracle_sample(w, 0.05, A, B, C, threads=1)
-    assert threads == 1 and gf > 0 and 1 <= n <= w["M"]
+    gf, dt, n, threads, check = bench.oracle_sample(w, 0.05, A, B, C, threads=1)
+    assert threads == 1 and gf > 0 and 1 <= n <= w["M"] and check is None
     assert oracle.max_threads() == full
+
+
+def test_result_check_against_the_oracle_rows():
+    # The bench's check compares the timed result with the oracle rows of its CPU sample: an
+    # exact result passes, one wrong cell fails it.
+    import oracle
+    w = bench.WORKLOADS["sq256_ab"]
+    A, B, C = bench.host_inputs(w)
+    full = oracle.sgemm(256, 256, 256, w["alpha"], A, 256, B, 256, w["beta"], C, 256)
+    gf, dt, n, threads, check = bench.oracle_sample(w, 0.05, A, B, C, result=full)
+    assert check["ok"] and check["normalized_error"] == 0.0 and check["rows"] >= 1
+    bad = full.copy()
+    bad[:, 7] += 1.0
+    _, _, _, _, check = bench.oracle_sample(w, 0.05, A, B, C, result=bad)
+    assert not check["ok"]
+
+
+def test_merge_clocks_prefers_nvml_and_unions_reasons():
+    nv = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 22}
+    smi = {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["hw_slowdown"], "samples": 2}
+    m = bench.merge_clocks(nv, smi)
+    assert m["sm_mhz"] == 2070.0 and m["samples"] == 22 and m["source"] == "nvml"
+    assert m["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    m = bench.merge_clocks({"sm_mhz": None, "samples": 0, "reasons": []}, smi)
+    assert m["source"] == "nvidia-smi" and m["sm_mhz"] == 2055.0
+
+
+def test_nvml_sampler_without_a_driver_reports_no_samples():
+    with bench.NvmlClocks(None, 0, 0.001) as nv:
+        pass
+    assert nv.summary()["samples"] >= 0
 
 
 def test_launches_per_call():
