@@ -1,6 +1,7 @@
 // config_table.h: per-shape-class choice of SIMT kernel configuration.
 //
-// Problems with one output dimension of at most 8 go to the HBM-streaming kernels (skinny_*).
+// Problems with one output dimension of at most 8 go to the HBM-streaming kernels (skinny_*),
+// and grids small enough for clusters of four or more CTAs to the cluster split-K kernels.
 // The rest fall into eight classes: operands TMA can read in place (16-byte aligned rows) or
 // not, times the grid depth in waves of 128 x 128 tiles at two CTAs per SM on the device's
 // multiprocessors (read at run time; 152 on a GB300):
@@ -37,6 +38,10 @@ enum : int {
     kCfgSkTma128x256k64 = 16,
     kCfgSkTma256x128k64 = 17,
     kCfgPackedSk256x128k64 = 18,
+    kCfgSplitK64 = 19,
+    kCfgCk128x256k64 = 20,
+    kCfgCk256x128k64 = 21,
+    kCfgPackedCk128x256k64 = 22,
 };
 
 // Shape classes, in the order of kClassWinner (config_table_gen.h) and of
@@ -83,11 +88,26 @@ inline int config_by_name(const char *name) {
 // taken as kDefaultSms): the bandwidth kernels for skinny shapes, else the measured winner of
 // the problem's shape class (falling back to a configuration that can run the problem when
 // the winner cannot, e.g. a broadcast batch that cannot be repacked).
+// Grids that form clusters of four or more CTAs under the cluster split-K schedule: more than
+// 512 x 512 output cells, 128 x 256 tiles numbering at most a quarter of the SMs, and at least
+// four 64-wide k-tiles. Measured on a GB300 (TFLOP/s, cluster split-K against the class's
+// stream-K winner): 1024^3 40.9 / 38.4, 1001 x 999 x 1003 (repacked) 30.2 / 26.6; with
+// clusters of two (1024 x 2048 x 1024: 46.6 / 50.7) or one (2048^3: 53.7 / 62.1) stream-K wins.
+inline bool clusterk_preferred(const SimtProblem &p, int sms) {
+    if (static_cast<long long>(p.M) * p.N * p.batch <= 512LL * 512) return false;
+    const long long tiles = static_cast<long long>((p.M + 127) / 128) * ((p.N + 255) / 256) * p.batch;
+    return tiles * 4 <= (sms > 0 ? sms : kDefaultSms) && (p.K + 63) / 64 >= 4;
+}
+
 inline int table_choose(const SimtProblem &p, int sms) {
     // One output dimension of at most 8: HBM-bound, the bandwidth kernels (any alignment).
     if (simt_config_supports(kCfgSkinnyTall, p)) return kCfgSkinnyTall;
     if (simt_config_supports(kCfgSkinnyWide, p)) return kCfgSkinnyWide;
     const bool tma = simt_config_supports(kCfgDpTma128x128, p);
+    if (clusterk_preferred(p, sms)) {
+        const int ck = tma ? kCfgCk128x256k64 : kCfgPackedCk128x256k64;
+        if (simt_config_supports(ck, p)) return ck;
+    }
     const int cls = shape_class(p, tma, sms);
     const int id = config_by_name(kClassWinner[cls]);
     if (id >= 0 && simt_config_supports(id, p)) return id;

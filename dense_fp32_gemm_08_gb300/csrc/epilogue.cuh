@@ -29,16 +29,23 @@ __device__ __forceinline__ float activate(float x, int act) {
     }
 }
 
-// One output value: alpha * acc (+ bias) -> act -> (+ beta * c). `c` is only dereferenced
-// when beta != 0.
-__device__ __forceinline__ float epilogue_value(float acc, float alpha, float beta,
+// One output value from an already loaded C value: alpha * acc (+ bias) -> act
+// (+ beta * c_value). c_value is ignored when beta == 0.
+__device__ __forceinline__ float epilogue_apply(float acc, float alpha, float beta,
                                                 const float *bias, int col, int act,
-                                                const float *c) {
+                                                float c_value) {
     float v = alpha * acc;
     if (bias) v += bias[col];
     v = activate(v, act);
-    if (beta != 0.0f) v = fmaf(beta, *c, v);
+    if (beta != 0.0f) v = fmaf(beta, c_value, v);
     return v;
+}
+
+// The same, reading C through `c`, which is only dereferenced when beta != 0.
+__device__ __forceinline__ float epilogue_value(float acc, float alpha, float beta,
+                                                const float *bias, int col, int act,
+                                                const float *c) {
+    return epilogue_apply(acc, alpha, beta, bias, col, act, beta != 0.0f ? *c : 0.0f);
 }
 
 }  // namespace sg

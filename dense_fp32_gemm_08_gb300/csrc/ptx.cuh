@@ -9,8 +9,32 @@ namespace sg {
 
 // Device error word: bit 0 = a bounded wait expired. Each translation unit that includes
 // this header has its own copy (internal linkage, no relocatable device code needed) and
-// exposes a host accessor that sgemm_device_status() reads and clears.
+// registers a reader for it when the library loads; sgemm_device_status() reads and clears
+// every registered word (take_fault_words).
 static __device__ unsigned int g_fault_word;
+
+// Host side of the fault words: the registry lives in sgemm_api.cu.
+using FaultWordReader = unsigned int (*)(cudaStream_t);
+void register_fault_word_reader(FaultWordReader reader);
+// Reads and clears every translation unit's fault word on the current device (synchronising
+// `stream`); returns their bitwise OR.
+unsigned int take_fault_words(cudaStream_t stream);
+
+namespace {
+// Reads and clears this translation unit's fault word on the current device.
+unsigned int take_unit_fault_word(cudaStream_t stream) {
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbolAsync(&word, g_fault_word, sizeof(word), 0, cudaMemcpyDeviceToHost,
+                                  stream) != cudaSuccess)
+        return 0;
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbolAsync(g_fault_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+    cudaStreamSynchronize(stream);
+    return word;
+}
+[[maybe_unused]] const bool g_unit_fault_word_registered =
+    (register_fault_word_reader(&take_unit_fault_word), true);
+}  // namespace
 
 constexpr unsigned int kFaultTimeout = 1u;
 // Wall-clock limit of one bounded wait, in ns of %globaltimer. A legitimate wait inside these

@@ -6,6 +6,8 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "config_table.h"
 #include "epilogue.cuh"
@@ -13,6 +15,35 @@
 #include "ptx.cuh"
 #include "simt_gemm.cuh"
 #include "tf32x3_gemm.cuh"
+
+namespace sg {
+namespace {
+std::mutex &fault_reader_mutex() {
+    static std::mutex m;
+    return m;
+}
+std::vector<FaultWordReader> &fault_readers() {
+    static std::vector<FaultWordReader> v;
+    return v;
+}
+}  // namespace
+
+void register_fault_word_reader(FaultWordReader reader) {
+    std::lock_guard<std::mutex> lock(fault_reader_mutex());
+    fault_readers().push_back(reader);
+}
+
+unsigned int take_fault_words(cudaStream_t stream) {
+    std::vector<FaultWordReader> readers;
+    {
+        std::lock_guard<std::mutex> lock(fault_reader_mutex());
+        readers = fault_readers();
+    }
+    unsigned int word = 0;
+    for (FaultWordReader read : readers) word |= read(stream);
+    return word;
+}
+}  // namespace sg
 
 namespace {
 
@@ -415,7 +446,7 @@ sgemm_status_t sgemm_device_status(void *stream_ptr) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     cudaError_t err = cudaStreamSynchronize(stream);
     if (err != cudaSuccess) return fail_cuda("stream synchronize", err);
-    const unsigned int word = sg::simt_take_fault_word(stream) | sg::tf32x3_take_fault_word(stream);
+    const unsigned int word = sg::take_fault_words(stream);
     if (word & sg::kFaultTimeout)
         return fail(SGEMM_ERR_TIMEOUT, "a bounded wait inside a kernel expired");
     return SGEMM_OK;

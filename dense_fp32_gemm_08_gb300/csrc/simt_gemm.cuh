@@ -19,6 +19,7 @@ enum ScheduleKind : int {
     kScheduleDataParallel = 0,  // one CTA per output tile (grouped raster order)
     kScheduleStreamK = 1,       // persistent CTAs, the last one-to-two waves split along K
     kSchedulePersistentDP = 2,  // persistent CTAs, whole tiles round-robin
+    kScheduleClusterK = 3,      // each tile split along K over a thread-block cluster
 };
 
 struct SimtConfig {
@@ -60,8 +61,6 @@ bool simt_config_supports(int id, const SimtProblem &p);
 // `detail` receives a static description of a failing step.
 cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const char **detail);
 
-// Reads and clears this file's device fault word on the current device.
-unsigned int simt_take_fault_word(cudaStream_t stream);
 
 // Frees every per-device workspace the SIMT kernels allocated (stream-K partial tiles).
 cudaError_t release_workspaces();

@@ -420,38 +420,42 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 if (row >= p.M || KB == 0) continue;
                 const int col0 = n0 + c0;
-                if (p.bias != nullptr || p.act != kActNone) {
+                const bool vec = p.c_vec4 && col0 + 31 < p.N;
+                // beta != 0: the slice's 32 C values are loaded before any store (a store may
+                // alias a later load as far as the compiler knows).
+                float cv[32];
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int col = col0 + jj;
-                        if (col < p.N)
-                            crow[col] = epilogue_value(v[jj], alpha, beta, p.bias, col, p.act,
-                                                       crow + col);
-                    }
-                } else if (p.c_vec4 && col0 + 31 < p.N) {
+                for (int jj = 0; jj < 32; ++jj) cv[jj] = 0.0f;
+                if (beta != 0.0f) {
+                    if (vec) {
 #pragma unroll
-                    for (int jj = 0; jj < 32; jj += 4) {
-                        float4 o;
-                        if (beta != 0.0f) {
+                        for (int jj = 0; jj < 32; jj += 4) {
                             const float4 c = *reinterpret_cast<const float4 *>(crow + col0 + jj);
-                            o = make_float4(fmaf(alpha, v[jj], beta * c.x),
-                                            fmaf(alpha, v[jj + 1], beta * c.y),
-                                            fmaf(alpha, v[jj + 2], beta * c.z),
-                                            fmaf(alpha, v[jj + 3], beta * c.w));
-                        } else {
-                            o = make_float4(alpha * v[jj], alpha * v[jj + 1], alpha * v[jj + 2],
-                                            alpha * v[jj + 3]);
+                            cv[jj] = c.x;
+                            cv[jj + 1] = c.y;
+                            cv[jj + 2] = c.z;
+                            cv[jj + 3] = c.w;
                         }
-                        *reinterpret_cast<float4 *>(crow + col0 + jj) = o;
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj)
+                            if (col0 + jj < p.N) cv[jj] = crow[col0 + jj];
                     }
+                }
+                const bool fused = p.bias != nullptr || p.act != kActNone;
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                    v[jj] = fused ? epilogue_apply(v[jj], alpha, beta, p.bias, col0 + jj, p.act, cv[jj])
+                                  : (beta != 0.0f ? fmaf(alpha, v[jj], beta * cv[jj]) : alpha * v[jj]);
+                if (vec) {
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj += 4)
+                        *reinterpret_cast<float4 *>(crow + col0 + jj) =
+                            make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
                 } else {
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int col = col0 + jj;
-                        if (col < p.N)
-                            crow[col] = beta != 0.0f ? fmaf(alpha, v[jj], beta * crow[col])
-                                                     : alpha * v[jj];
-                    }
+                    for (int jj = 0; jj < 32; ++jj)
+                        if (col0 + jj < p.N) crow[col0 + jj] = v[jj];
                 }
             }
         }
@@ -766,15 +770,5 @@ cudaError_t tf32x3_release_workspaces() {
     return first;
 }
 
-unsigned int tf32x3_take_fault_word(cudaStream_t stream) {
-    unsigned int word = 0;
-    if (cudaMemcpyFromSymbolAsync(&word, g_fault_word, sizeof(word), 0, cudaMemcpyDeviceToHost,
-                                  stream) != cudaSuccess)
-        return 0;
-    const unsigned int zero = 0;
-    cudaMemcpyToSymbolAsync(g_fault_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
-    cudaStreamSynchronize(stream);
-    return word;
-}
 
 }  // namespace sg

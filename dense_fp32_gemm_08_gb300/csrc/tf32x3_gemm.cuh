@@ -16,7 +16,6 @@ cudaError_t tf32x3_launch(const SimtProblem &p, cudaStream_t stream, const char 
 // One TF32 product per multiply-add (operands rounded to TF32): the fast, lower-accuracy mode.
 cudaError_t tf32_launch(const SimtProblem &p, cudaStream_t stream, const char **detail);
 
-unsigned int tf32x3_take_fault_word(cudaStream_t stream);
 
 // Frees the per-(device, stream) workspaces holding the split operands.
 cudaError_t tf32x3_release_workspaces();
