@@ -11,10 +11,12 @@ SMS = 152
 # class name -> (representative (M, N, K) shapes, candidate configuration names)
 ALIGNED = ["dp_tma_128x128_s3", "dp_tma_128x256_s4", "sk_tma_ws_128x128_s3", "sk_tma_ws_128x256_s4",
            "sk_tma_ws_256x128_s4", "pdp_tma_ws_128x256_s4", "sk_tma_ws_128x256_k64_s2",
-           "sk_tma_ws_256x128_k64_s2", "splitk_cpasync_64x64"]
+           "sk_tma_ws_256x128_k64_s2", "splitk_cpasync_64x64", "ck_tma_128x256_k64_s2",
+           "ck_tma_256x128_k64_s2"]
 UNALIGNED = ["packed_sk_tma_128x256_s4", "packed_dp_tma_128x128_s3", "packed_sk_tma_256x128_k64_s2",
              "sk_cpasync_128x256_s4",
-             "dp_cpasync_128x256_s4", "dp_cpasync_128x128_s3", "splitk_cpasync_64x64"]
+             "dp_cpasync_128x256_s4", "dp_cpasync_128x128_s3", "splitk_cpasync_64x64",
+             "packed_ck_tma_128x256_k64_s2"]
 
 CLASSES = {
     "aligned_tiny": ([(128, 128, 128), (256, 256, 256), (512, 512, 512), (128, 64, 2048)], ALIGNED),
@@ -46,3 +48,22 @@ def classify(M: int, N: int, aligned: bool, batch: int = 1, sms: int = SMS) -> s
     if w < 6.0:
         return prefix + "_medium"
     return prefix + "_large"
+
+
+def clusterk_preferred(M: int, N: int, K: int, batch: int = 1, sms: int = SMS) -> bool:
+    """Grids that take the cluster split-K kernel ahead of the class table (mirrors
+    clusterk_preferred in config_table.h): more than 512 x 512 outputs, at most sms / 4 tiles
+    of 128 x 256, at least four 64-wide k-tiles."""
+    if M * N * batch <= 512 * 512:
+        return False
+    tiles = ((M + 127) // 128) * ((N + 255) // 256) * batch
+    return tiles * 4 <= sms and (K + 63) // 64 >= 4
+
+
+def expected_config(M: int, N: int, K: int, aligned: bool, winners: dict, batch: int = 1,
+                    sms: int = SMS) -> str:
+    """The configuration the library picks for a non-skinny problem: the cluster split-K
+    kernel where clusterk_preferred holds, else the class's measured winner."""
+    if clusterk_preferred(M, N, K, batch, sms):
+        return "ck_tma_128x256_k64_s2" if aligned else "packed_ck_tma_128x256_k64_s2"
+    return winners[classify(M, N, aligned, batch, sms)]

@@ -27,6 +27,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=str(HERE / "measured.json"))
     ap.add_argument("--reps", type=int, default=10)
+    ap.add_argument("--classes", nargs="*", default=None,
+                    help="re-measure only these classes, keeping the others from --out")
     args = ap.parse_args(argv)
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
@@ -35,8 +37,13 @@ def main(argv=None):
     result = {"device": torch.cuda.get_device_name(0),
               "sms": torch.cuda.get_device_properties(0).multi_processor_count,
               "when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()), "classes": {}}
+    if args.classes and Path(args.out).exists():
+        kept = json.loads(Path(args.out).read_text())["classes"]
+        result["classes"] = {c: v for c, v in kept.items() if c not in args.classes}
     try:
         for cls, (shapes, candidates) in CLASSES.items():
+            if args.classes and cls not in args.classes:
+                continue
             per_cfg = {}
             for (M, N, K) in shapes:
                 A = torch.randn(M, K, device=dev)
@@ -73,6 +80,7 @@ def main(argv=None):
             print(cls, result["classes"][cls]["winner"], means, flush=True)
     finally:
         sg.sgemm_force_config(-1)
+    result["classes"] = {c: result["classes"][c] for c in CLASSES if c in result["classes"]}
     Path(args.out).write_text(json.dumps(result, indent=1) + "\n")
 
 

@@ -154,7 +154,7 @@ def test_skinny_strided_batched(sg, M, N, K, batch):
 
 # ---- every configuration of the table ---------------------------------------------------------
 
-@pytest.mark.parametrize("cfg", range(20))
+@pytest.mark.parametrize("cfg", range(23))
 @pytest.mark.parametrize("shape", [(640, 768, 544), (257, 383, 129), (128, 256, 32),
                                    (4096, 2560, 320), (1000, 3000, 2000)])
 def test_each_config(sg, cfg, shape):
@@ -191,6 +191,32 @@ def test_stream_k_deterministic_and_exact(sg, name):
         # unaligned leading dimensions (cp.async loaders take them; TMA ones fall back)
         _check(Case(4095, 3001, 1537, 0.7, -1.3, "normal", seed=13, rows=sample_rows(4095)), sg)
         _check(Case(127, 129, 4099, 0.7, -1.3, "normal", seed=14), sg)
+    finally:
+        sg.sgemm_force_config(-1)
+
+
+@pytest.mark.parametrize("name", ["ck_tma_128x256_k64_s2", "ck_tma_256x128_k64_s2",
+                                  "packed_ck_tma_128x256_k64_s2"])
+def test_cluster_k_deterministic_and_exact(sg, name):
+    """Cluster split-K: every tile's K slices are added through distributed shared memory in
+    rank order, so repeated runs agree bit for bit; small integers are exact. The shapes give
+    clusters of 8, 4, 2 and 1 CTAs, fewer k-tiles than slices, ragged edges and a batch."""
+    ids = {sg.sgemm_config_name(i): i for i in range(sg.sgemm_num_configs())}
+    sg.sgemm_force_config(ids[name])
+    try:
+        for M, N, K in [(1024, 1024, 1024), (512, 512, 2048), (300, 520, 700), (257, 383, 129),
+                        (128, 256, 32), (2048, 2048, 512)]:
+            case = Case(M, N, K, 0.7, -1.3, "normal", seed=M + K)
+            err, first, _ = run(case, sg.sgemm, torch)
+            assert err <= TOL
+            _, second, _ = run(case, sg.sgemm, torch, check=False)
+            assert np.array_equal(first, second), "cluster split-K result differs between runs"
+            got, ref = _check(Case(M, N, K, 1.0, -1.0, "small_int", seed=M + N), sg)
+            assert np.array_equal(got, ref)
+        _check(Case(333, 291, 457, 0.7, -1.3, "normal", seed=7, lda_pad=4, ldb_pad=8, ldc_pad=3,
+                    c_off=3), sg)
+        _batched(sg, 256, 320, 200, 3, 256 * 200, 200 * 320, 256 * 320, 0.7, -1.3,
+                 sg.sgemm_strided_batched)
     finally:
         sg.sgemm_force_config(-1)
 

@@ -28,13 +28,22 @@ def test_library_follows_the_class_table(sgemm_lib):
     sel, name = sgemm_lib.sgemm_select_config, sgemm_lib.sgemm_config_name
     shapes = [(96, 96, 512), (512, 512, 512), (2048, 2048, 2048), (4096, 4096, 4096),
               (4096, 3072, 2048), (8192, 8192, 8192), (16384, 12288, 4096), (300, 9000, 64)]
-    for (M, N, K) in shapes:
-        cls = classes.classify(M, N, aligned=True)
-        assert name(sel(M, N, K, 1.0, FAKE, K, FAKE, N, FAKE, N)) == measured["classes"][cls]["winner"]
+    winners = {c: v["winner"] for c, v in measured["classes"].items()}
+    for (M, N, K) in shapes + [(1024, 1024, 1024), (768, 1536, 512), (1024, 2048, 1024)]:
+        want = classes.expected_config(M, N, K, True, winners)
+        assert name(sel(M, N, K, 1.0, FAKE, K, FAKE, N, FAKE, N)) == want, (M, N, K)
     for (M, N, K) in [(97, 95, 513), (1001, 999, 1003), (4095, 3001, 1537), (8191, 8193, 8195)]:
-        cls = classes.classify(M, N, aligned=False)
         got = name(sel(M, N, K, 1.0, FAKE, K, FAKE, N, FAKE, N))
-        assert got == measured["classes"][cls]["winner"], (M, N, K, cls)
+        assert got == classes.expected_config(M, N, K, False, winners), (M, N, K)
+
+
+def test_cluster_split_k_rule():
+    assert classes.clusterk_preferred(1024, 1024, 1024)          # 32 tiles: clusters of 4
+    assert not classes.clusterk_preferred(1024, 2048, 1024)      # 64 tiles: clusters of 2
+    assert not classes.clusterk_preferred(512, 512, 512)         # tiny: the one-warp kernel
+    assert not classes.clusterk_preferred(1024, 1024, 192)       # three 64-wide k-tiles
+    assert classes.clusterk_preferred(1024, 1024, 1024, sms=152)
+    assert not classes.clusterk_preferred(1024, 1024, 1024, sms=76)
 
 
 @pytest.mark.parametrize("M,N,aligned,want", [(64, 64, True, "aligned_tiny"),
