@@ -8,8 +8,11 @@ beta = 0 (the pages' headline problem, 137.4 GFLOP per call). A "step" is one li
                   [--path simt|3xtf32|tf32] [--no-paths] [--no-sweep]
 
 Timing: W untimed warm-up steps, then exactly K steps. Before every step a 256 MiB buffer is
-written (L2 is 129 MB) so each step starts with cold L2; each step's GEMM is bracketed by CUDA
-events on the stream it runs on. value = 2*M*N*K * K_steps * ranks / max over ranks of the
+written (L2 is 129 MB), so each step starts with cold L2, and another 256 MiB buffer is read,
+so the lines the write left dirty are written back before the step rather than during it;
+each step's GEMM is bracketed by CUDA events on the stream it runs on. A spin kernel ahead of
+the steps keeps the device busy while the host queues them, so host-side delays never fall
+between a start event and its launch. value = 2*M*N*K * K_steps * ranks / max over ranks of the
 summed GEMM time. SM clocks and clock-event reasons are sampled in process through NVML every
 2 ms during the timed steps (nvidia-smi every 20 ms as well); a `sustained` block then repeats
 the step for at least one second under the same sampling. Under torchrun (N > 1) every rank
@@ -19,8 +22,11 @@ is on the data path) and the max of the per-rank times is taken through the proc
 After the headline line's own measurement (and outside its timed region) the same run reports
 `paths` (the 3xTF32 and TF32 tensor-core paths on the same workload, against the TF32 peak)
 and `sweep` (the square sizes 128..16384, the four edge shapes and the four LLM-layer shapes
-on the SIMT path, each with cuBLAS SGEMM timed beside it under the same rules). Sweep inputs
-are drawn on the device from torch's seeded generator with the workloads' distributions.
+on the SIMT path, each with cuBLAS SGEMM timed beside it under the same rules; the HBM-bound
+shapes also against a device copy that reads the same bytes, the copy peak's method at that
+size).
+Sweep inputs are drawn on the device from torch's seeded generator with the workloads'
+distributions.
 
 The CPU baseline times the oracle on a row sample of the workload; the same rows of the
 timed call's result are compared with the oracle's (the `check` block) and the run fails
@@ -409,11 +415,39 @@ def device_inputs(torch, dev, w, seed=0):
     return draw(M, K, w["dist"]), draw(K, N, w["dist"]), draw(M, N, w["dist"])
 
 
+class L2Flush:
+    """Before every timed call: write a 256 MiB buffer (evicts the call's inputs from the
+    129 MB L2), then read another 256 MiB buffer, so the lines the write left dirty are written
+    back now rather than by the timed call's first evictions. The call starts cold and clean."""
+
+    def __init__(self, torch, dev, nbytes=L2_FLUSH_BYTES):
+        self.dirty = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+        self.clean = torch.ones(nbytes // 4, dtype=torch.float32, device=dev)
+
+    def fill_(self, value):
+        self.dirty.fill_(value)
+        self.clean.sum()
+        return self
+
+    describe = "flushed before every step: 256 MiB written, then 256 MiB read (cold, clean L2)"
+
+
+def hold_device(torch, n):
+    """Keeps the device busy (a spin kernel of about 0.2 ms per step to come, at most 20 ms)
+    while the host queues the next n steps, so that no host-side delay between a step's
+    start event and its launch (Python, the binding, a clock sample) lands inside the timed
+    window: every step then starts as soon as the previous work on the stream ends."""
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        sleep(int(min(2e8, 4e5 * n + 1e6)))   # cycles, ~2 GHz
+
+
 def time_steps(torch, stream, step, n, flush, restore=None):
     """Runs `step` n times, each after an L2 flush (and `restore`, e.g. C <- C0), and returns
     each call's device time in ms (CUDA events on `stream` around the call only)."""
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    hold_device(torch, n)
     for i in range(n):
         flush.fill_(float(i))
         if restore is not None:
@@ -473,7 +507,7 @@ def run_ours(args):
     B = torch.from_numpy(B_h).to(dev)
     C = torch.from_numpy(C_h).to(dev)
     C0 = C.clone() if beta != 0.0 else None
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
     cfg_id = sg.sgemm_select_config(M, N, K, alpha, A, K, B, N, C, N)
     kernel = (sg.sgemm_config_name(cfg_id) if args.path == "simt"
@@ -549,7 +583,7 @@ def run_ours(args):
         "config": {"workload": workload_name(args.workload, w), "M": M, "N": N, "K": K,
                    "alpha": alpha, "beta": beta, "inputs": w["dist"] + ", seed 0",
                    "path": args.path, "kernel": kernel,
-                   "l2": "flushed before every step (256 MiB write)",
+                   "l2": L2Flush.describe,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "gflops_median": round(flops / (statistics.median(step_ms) / 1e3) / 1e9, 1),
         "gflops_best": round(flops / (min(step_ms) / 1e3) / 1e9, 1),
@@ -621,6 +655,23 @@ def measure_paths(args, torch, sg, stream, w, A, B, C, restore, flush, sms):
     return out
 
 
+def size_matched_copy(torch, dev, stream, flush, nbytes, n):
+    """The HBM roof for a call that reads `nbytes`, under the same flush and events: a device
+    copy (the measured peak's method) that reads the same bytes, nbytes into nbytes. At tens
+    of MB the launch and ramp of any kernel are a large part of the time; a copy that reads
+    only half the bytes would understate the roof for reads, since the L2 (write-back, 129 MB)
+    absorbs its writes during the call."""
+    src = torch.ones(max(1, nbytes // 4), dtype=torch.float32, device=dev)
+    dst = torch.empty_like(src)
+    for _ in range(2):
+        flush.fill_(1.0)
+        dst.copy_(src)
+    ms = time_steps(torch, stream, lambda: dst.copy_(src), n, flush)
+    avg = sum(ms) / len(ms)
+    return {"ms": round(avg, 4), "read_gbs": round(4 * src.numel() / (avg / 1e3) / 1e9, 1),
+            "how": "torch copy reading the call's bytes into another buffer, same flush and events"}
+
+
 SWEEP = ([f"sweep{n}" for n in (128, 256, 512, 1024, 2048, 4096, 8192, 16384)] +
          ["edge0", "edge1", "edge2", "edge3", "llm_qkv", "llm_up", "llm_down", "llm_head"])
 
@@ -661,12 +712,14 @@ def measure_sweep(torch, sg, dev, stream, flush, sms, steps):
             hbm = measured_peaks().get("hbm_gbs")
             if hbm:
                 row["pct_hbm_measured"] = round(100.0 * row["gbs"] / hbm, 2)
+            row["size_matched_copy"] = size_matched_copy(torch, dev, stream, flush, nbytes, n)
+            row["frac_of_size_matched_copy"] = round(row["size_matched_copy"]["ms"] / avg, 4)
         rows.append(row)
         del A, B, C, C0
         torch.cuda.empty_cache()
     return {"path": "simt", "inputs": "device-drawn from torch's seeded generator (seed 0), "
                                       "the workloads' distributions",
-            "l2": "flushed before every call (256 MiB write)", "rows": rows}
+            "l2": L2Flush.describe, "rows": rows}
 
 
 def launches_per_call(path: str, kernel: str, w) -> int:

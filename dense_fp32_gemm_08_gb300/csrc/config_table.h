@@ -42,6 +42,8 @@ enum : int {
     kCfgCk128x256k64 = 20,
     kCfgCk256x128k64 = 21,
     kCfgPackedCk128x256k64 = 22,
+    kCfgCk128x256s4 = 23,
+    kCfgCk256x128s4 = 24,
 };
 
 // Shape classes, in the order of kClassWinner (config_table_gen.h) and of
@@ -93,6 +95,8 @@ inline int config_by_name(const char *name) {
 // four 64-wide k-tiles. Measured on a GB300 (TFLOP/s, cluster split-K against the class's
 // stream-K winner): 1024^3 40.9 / 38.4, 1001 x 999 x 1003 (repacked) 30.2 / 26.6; with
 // clusters of two (1024 x 2048 x 1024: 46.6 / 50.7) or one (2048^3: 53.7 / 62.1) stream-K wins.
+// Aligned operands take the 32-wide-stage variant (its first stage lands sooner: 1024^3
+// 53.9 us against 54.6 us for the 64-wide one).
 inline bool clusterk_preferred(const SimtProblem &p, int sms) {
     if (static_cast<long long>(p.M) * p.N * p.batch <= 512LL * 512) return false;
     const long long tiles = static_cast<long long>((p.M + 127) / 128) * ((p.N + 255) / 256) * p.batch;
@@ -105,7 +109,7 @@ inline int table_choose(const SimtProblem &p, int sms) {
     if (simt_config_supports(kCfgSkinnyWide, p)) return kCfgSkinnyWide;
     const bool tma = simt_config_supports(kCfgDpTma128x128, p);
     if (clusterk_preferred(p, sms)) {
-        const int ck = tma ? kCfgCk128x256k64 : kCfgPackedCk128x256k64;
+        const int ck = tma ? kCfgCk128x256s4 : kCfgPackedCk128x256k64;
         if (simt_config_supports(ck, p)) return ck;
     }
     const int cls = shape_class(p, tma, sms);

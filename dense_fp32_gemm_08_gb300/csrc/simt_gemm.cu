@@ -176,6 +176,8 @@ const SimtConfig kConfigs[] = {
     {"ck_tma_128x256_k64_s2", 128, 256, 2, 4, 2, kLoaderTma, kScheduleClusterK},
     {"ck_tma_256x128_k64_s2", 256, 128, 4, 2, 2, kLoaderTma, kScheduleClusterK},
     {"packed_ck_tma_128x256_k64_s2", 128, 256, 2, 4, 2, kLoaderTma, kScheduleClusterK},
+    {"ck_tma_128x256_s4", 128, 256, 2, 4, 4, kLoaderTma, kScheduleClusterK},
+    {"ck_tma_256x128_s4", 256, 128, 4, 2, 4, kLoaderTma, kScheduleClusterK},
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 
@@ -222,7 +224,7 @@ cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const
         case 16: case 17: return simt_launch_sk64(id, p, stream, detail);
         case 18: return launch_packed(17, p, stream, detail);
         case 19: return launch_small_splitk(p, stream, detail);
-        case 20: case 21: return simt_launch_ck(id, p, stream, detail);
+        case 20: case 21: case 23: case 24: return simt_launch_ck(id, p, stream, detail);
         case 22: return launch_packed(20, p, stream, detail);
         default: *detail = "unknown SIMT configuration"; return cudaErrorInvalidValue;
     }

@@ -9,6 +9,8 @@ cudaError_t simt_launch_ck(int id, const SimtProblem &p, cudaStream_t stream, co
     switch (id) {
         case 20: return launch_clusterk<128, 256, 2, 4, 2, 2>(p, stream, detail);
         case 21: return launch_clusterk<256, 128, 4, 2, 2, 2>(p, stream, detail);
+        case 23: return launch_clusterk<128, 256, 2, 4, 4, 1>(p, stream, detail);
+        case 24: return launch_clusterk<256, 128, 4, 2, 4, 1>(p, stream, detail);
         default: *detail = "configuration not in this kernel unit"; return cudaErrorInvalidValue;
     }
 }

@@ -12,7 +12,7 @@ SMS = 152
 ALIGNED = ["dp_tma_128x128_s3", "dp_tma_128x256_s4", "sk_tma_ws_128x128_s3", "sk_tma_ws_128x256_s4",
            "sk_tma_ws_256x128_s4", "pdp_tma_ws_128x256_s4", "sk_tma_ws_128x256_k64_s2",
            "sk_tma_ws_256x128_k64_s2", "splitk_cpasync_64x64", "ck_tma_128x256_k64_s2",
-           "ck_tma_256x128_k64_s2"]
+           "ck_tma_256x128_k64_s2", "ck_tma_128x256_s4", "ck_tma_256x128_s4"]
 UNALIGNED = ["packed_sk_tma_128x256_s4", "packed_dp_tma_128x128_s3", "packed_sk_tma_256x128_k64_s2",
              "sk_cpasync_128x256_s4",
              "dp_cpasync_128x256_s4", "dp_cpasync_128x128_s3", "splitk_cpasync_64x64",
@@ -65,5 +65,5 @@ def expected_config(M: int, N: int, K: int, aligned: bool, winners: dict, batch:
     """The configuration the library picks for a non-skinny problem: the cluster split-K
     kernel where clusterk_preferred holds, else the class's measured winner."""
     if clusterk_preferred(M, N, K, batch, sms):
-        return "ck_tma_128x256_k64_s2" if aligned else "packed_ck_tma_128x256_k64_s2"
+        return "ck_tma_128x256_s4" if aligned else "packed_ck_tma_128x256_k64_s2"
     return winners[classify(M, N, aligned, batch, sms)]

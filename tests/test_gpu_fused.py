@@ -82,7 +82,7 @@ def test_fused_epilogue(sgemm_lib, path, act, with_bias, alpha, beta):
     _run(sgemm_lib, 384, 640, 512, alpha, beta, act, with_bias, path=path, seed=7)
 
 
-@pytest.mark.parametrize("cfg", range(23))
+@pytest.mark.parametrize("cfg", range(25))
 def test_fused_every_config(sgemm_lib, cfg):
     sg = sgemm_lib
     if cfg >= sg.sgemm_num_configs():

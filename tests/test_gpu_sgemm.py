@@ -154,7 +154,7 @@ def test_skinny_strided_batched(sg, M, N, K, batch):
 
 # ---- every configuration of the table ---------------------------------------------------------
 
-@pytest.mark.parametrize("cfg", range(23))
+@pytest.mark.parametrize("cfg", range(25))
 @pytest.mark.parametrize("shape", [(640, 768, 544), (257, 383, 129), (128, 256, 32),
                                    (4096, 2560, 320), (1000, 3000, 2000)])
 def test_each_config(sg, cfg, shape):
@@ -196,7 +196,8 @@ def test_stream_k_deterministic_and_exact(sg, name):
 
 
 @pytest.mark.parametrize("name", ["ck_tma_128x256_k64_s2", "ck_tma_256x128_k64_s2",
-                                  "packed_ck_tma_128x256_k64_s2"])
+                                  "packed_ck_tma_128x256_k64_s2", "ck_tma_128x256_s4",
+                                  "ck_tma_256x128_s4"])
 def test_cluster_k_deterministic_and_exact(sg, name):
     """Cluster split-K: every tile's K slices are added through distributed shared memory in
     rank order, so repeated runs agree bit for bit; small integers are exact. The shapes give
