@@ -277,8 +277,10 @@ def merge_clocks(nvml: dict, smi: dict) -> dict:
 # ---- profiles (ncu traffic figures committed under profiles/) --------------------------------------
 
 KERNEL_SOURCES = {
-    "simt": ("simt_gemm.cu", "simt_gemm.cuh", "ptx.cuh"),
-    "3xtf32": ("tf32x3_gemm.cu", "tf32x3_gemm.cuh", "ptx.cuh"),
+    "simt": ("simt_kernels.cuh", "simt_gemm.cu", "simt_gemm_dp.cu", "simt_gemm_dpcp.cu",
+             "simt_gemm_sk.cu", "simt_gemm_sk128.cu", "simt_gemm_sk64.cu", "simt_gemm_skcp.cu",
+             "simt_gemm_ck.cu", "simt_gemm.cuh", "ptx.cuh", "epilogue.cuh", "raster.cuh"),
+    "3xtf32": ("tf32x3_gemm.cu", "tf32x3_gemm.cuh", "ptx.cuh", "epilogue.cuh", "raster.cuh"),
 }
 
 
