@@ -245,6 +245,27 @@ __device__ __forceinline__ void cp_async_stage(float *sA, float *sB, const KPara
 // trip per value. The plain form loads CHUNKS 4-column chunks at a time, the fused form (whose
 // activation needs registers of its own) one chunk at a time; more at once spills registers
 // in the persistent kernels.
+// With beta != 0, asks L2 to fetch the C values the thread's epilogue will read (its 8 rows x
+// 16 columns, valid addresses only), so that the epilogue's loads hit L2 instead of waiting on
+// DRAM. Issued just before the epilogue (and the stream-K fix-up): the prefetches are
+// fire-and-forget, so the epilogue's load rounds after the first find their lines already on
+// the way. A prefetch is a hint and changes no value.
+__device__ __forceinline__ void prefetch_c(const KParams &p, const float *Cb, int row0, int col0) {
+    if (p.beta == 0.0f) return;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int gm = row0 + 8 * r;
+        if (gm >= p.M) continue;
+        const float *crow = Cb + static_cast<long long>(gm) * p.ldc;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int gn = col0 + 16 * q;
+            if (gn < p.N)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(crow + gn) : "memory");
+        }
+    }
+}
+
 __device__ __forceinline__ void load_c4(const KParams &p, const float *crow, int gn, float (&c)[4]) {
     if (p.c_vec4 && gn + 3 < p.N) {
         const float4 v = *reinterpret_cast<const float4 *>(crow + gn);
@@ -428,6 +449,7 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32, 1)
             __syncthreads();
         }
         if (s_abort) break;
+        prefetch_c(p, p.C + static_cast<long long>(b) * p.sC, m0 + wm0 + tr, n0 + wn0 + 4 * tc);
         epilogue(p, p.C + static_cast<long long>(b) * p.sC, m0 + wm0 + tr, n0 + wn0 + 4 * tc, acc);
     }
 
@@ -711,6 +733,10 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
             if (lane == 0) st_release_gpu(&p.flags[cta * WARPS + warp], p.epoch);
             continue;
         }
+        // This CTA finishes the tile: start C's way into L2 while the fix-up (if any) runs, so
+        // the epilogue's load rounds after the first find their lines arriving.
+        prefetch_c(p.k, p.k.C + static_cast<long long>(b) * p.k.sC, m0 + wm0 + tr,
+                   n0 + wn0 + 4 * tc);
         if (seg.k0 > 0) {
             // Owner of a split tile: add the pieces of the lower-numbered CTAs that hold
             // k-iterations [0, k0) of this tile, highest-numbered (latest k) first.
