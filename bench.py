@@ -726,11 +726,11 @@ def measure_sweep(torch, sg, dev, stream, flush, sms, steps):
 
 def launches_per_call(path: str, kernel: str, w) -> int:
     """Kernels one library call launches for the bench's operands (lda = K, ldb = N,
-    ldc = N, 16-byte-aligned allocations): the tensor paths split A, split-and-transpose B,
-    then run the GEMM; a repacked SIMT configuration first copies each operand whose rows
-    TMA cannot read (K or N not a multiple of 4) into aligned storage."""
+    ldc = N, 16-byte-aligned allocations): the tensor paths split (or round) both operands in
+    one launch, then run the GEMM; a repacked SIMT configuration first copies each operand
+    whose rows TMA cannot read (K or N not a multiple of 4) into aligned storage."""
     if path in ("3xtf32", "tf32"):
-        return 3
+        return 2
     n = 1
     if kernel.startswith("packed"):
         n += int(w["K"] % 4 != 0) + int(w["N"] % 4 != 0)

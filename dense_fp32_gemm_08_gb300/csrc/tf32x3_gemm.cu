@@ -78,22 +78,38 @@ __device__ __forceinline__ void split_value(float x, float &big, float &small) {
     }
 }
 
-// A (rows x cols, leading dimension lda, batch stride sA) -> big, small (rows x ldo each,
-// batch stride so; ldo and so multiples of 4, outputs 16-byte aligned), same orientation.
-// Rows over the grid's y dimension, columns over threads; float4 access when A allows.
-template <bool VEC, bool SMALL>
-__global__ void split_rows_kernel(const float *__restrict__ A, long long lda, long long sA,
-                                  float *__restrict__ big, float *__restrict__ small,
-                                  long long ldo, long long so, int rows, int cols, int batch) {
-    const long long nrows = static_cast<long long>(rows) * batch;
-    const int stride = gridDim.x * blockDim.x;
-    for (long long gr = blockIdx.y; gr < nrows; gr += gridDim.y) {
-        const long long b = gr / rows, r = gr - b * rows;
-        const float *src = A + b * sA + r * lda;
-        float *hi = big + b * so + r * ldo;
-        float *lo = small + b * so + r * ldo;
-        const int c4 = VEC ? (cols & ~3) : 0;
-        for (int c = 4 * (blockIdx.x * blockDim.x + threadIdx.x); c < c4; c += 4 * stride) {
+// One operand's share of the split pre-pass. A rows job keeps the orientation: src (rows x
+// cols, leading dimension ld, batch stride stride) -> big, small (rows x ldo each, batch
+// stride so; ldo and so multiples of 4, outputs 16-byte aligned). A transposing job writes
+// src (rows = K x cols = N) as N x K (K contiguous). Both operands' jobs run in one launch:
+// CTAs [0, j0.blocks) take the first job, the rest the second.
+struct SplitJob {
+    const float *src;
+    long long ld, stride;
+    float *big, *small;
+    long long ldo, so;
+    int rows, cols, batch;
+    int transpose;  // 0: rows job, 1: transposing job
+    int vec;        // 16-byte source reads allowed
+    int gx, gy;     // the job's CTA grid: rows job gx x gy; transposing job gx x gy x batch
+    long long blocks;
+};
+
+// Rows job: rows over the grid's y dimension, columns over threads, float4 access when the
+// source allows.
+template <bool SMALL>
+__device__ __forceinline__ void split_rows(const SplitJob &j, long long bid) {
+    const int bx = static_cast<int>(bid % j.gx);
+    const long long by = bid / j.gx;
+    const long long nrows = static_cast<long long>(j.rows) * j.batch;
+    const int stride = j.gx * blockDim.x;
+    for (long long gr = by; gr < nrows; gr += j.gy) {
+        const long long b = gr / j.rows, r = gr - b * j.rows;
+        const float *src = j.src + b * j.stride + r * j.ld;
+        float *hi = j.big + b * j.so + r * j.ldo;
+        float *lo = j.small + b * j.so + r * j.ldo;
+        const int c4 = j.vec ? (j.cols & ~3) : 0;
+        for (int c = 4 * (bx * blockDim.x + threadIdx.x); c < c4; c += 4 * stride) {
             const float4 x = __ldcs(reinterpret_cast<const float4 *>(src + c));
             float4 h, l;
             split_value(x.x, h.x, l.x);
@@ -103,7 +119,7 @@ __global__ void split_rows_kernel(const float *__restrict__ A, long long lda, lo
             *reinterpret_cast<float4 *>(hi + c) = h;
             if (SMALL) *reinterpret_cast<float4 *>(lo + c) = l;
         }
-        for (int c = c4 + blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += stride) {
+        for (int c = c4 + bx * blockDim.x + threadIdx.x; c < j.cols; c += stride) {
             float h, l;
             split_value(src[c], h, l);
             hi[c] = h;
@@ -112,26 +128,26 @@ __global__ void split_rows_kernel(const float *__restrict__ A, long long lda, lo
     }
 }
 
-// B (K x N, ldb, batch stride sB) -> transposed big, small (N x ldo, K contiguous). A 32 x 32
-// tile goes through shared memory: 256 threads each read one float4 along n (when B allows)
-// and write one float4 along k of each output, so both sides move 16 bytes per thread.
-template <bool VEC, bool SMALL>
-__global__ void __launch_bounds__(256)
-    split_transpose_kernel(const float *__restrict__ B, long long ldb, long long sB,
-                           float *__restrict__ big, float *__restrict__ small, long long ldo,
-                           long long so, int K, int N) {
-    __shared__ float tile[32][33];
-    const int b = blockIdx.z;
-    const int n0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+// Transposing job: a 32 x 32 tile goes through shared memory; 256 threads each read one
+// float4 along n (when the source allows) and write one float4 along k of each output, so
+// both sides move 16 bytes per thread.
+template <bool SMALL>
+__device__ __forceinline__ void split_transpose(const SplitJob &j, long long bid,
+                                                float (&tile)[32][33]) {
+    const int K = j.rows, N = j.cols;
+    const int n0 = static_cast<int>(bid % j.gx) * 32;
+    const long long rest = bid / j.gx;
+    const int k0 = static_cast<int>(rest % j.gy) * 32;
+    const long long b = rest / j.gy;
     const int t = threadIdx.x;
-    const float *Bb = B + b * sB;
+    const float *Bb = j.src + b * j.stride;
     {
         const int kr = t >> 3, nc = (t & 7) * 4;  // row k0 + kr, columns n0 + nc .. + 3
         const int k = k0 + kr, n = n0 + nc;
         float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         if (k < K) {
-            const float *src = Bb + static_cast<long long>(k) * ldb + n;
-            if (VEC && n + 3 < N) {
+            const float *src = Bb + static_cast<long long>(k) * j.ld + n;
+            if (j.vec && n + 3 < N) {
                 v = __ldcs(reinterpret_cast<const float4 *>(src));
             } else {
                 if (n < N) v.x = src[0];
@@ -155,8 +171,8 @@ __global__ void __launch_bounds__(256)
             split_value(tile[kc + 1][nr], h.y, l.y);
             split_value(tile[kc + 2][nr], h.z, l.z);
             split_value(tile[kc + 3][nr], h.w, l.w);
-            float *ob = big + b * so + static_cast<long long>(n) * ldo + k;
-            float *os = small + b * so + static_cast<long long>(n) * ldo + k;
+            float *ob = j.big + b * j.so + static_cast<long long>(n) * j.ldo + k;
+            float *os = j.small + b * j.so + static_cast<long long>(n) * j.ldo + k;
             if (k + 3 < K) {
                 *reinterpret_cast<float4 *>(ob) = h;
                 if (SMALL) *reinterpret_cast<float4 *>(os) = l;
@@ -169,6 +185,23 @@ __global__ void __launch_bounds__(256)
             }
         }
     }
+}
+
+// Both operands' split in one launch. The GEMM that follows is launched as a programmatic
+// dependent: every CTA here lets it start its prologue at once, and it waits for this grid's
+// completion (griddepcontrol.wait) before it reads a split operand.
+template <bool SMALL>
+__global__ void __launch_bounds__(256) split_operands_kernel(const SplitJob j0, const SplitJob j1) {
+    __shared__ float tile[32][33];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    long long bid = blockIdx.x;
+    const bool first = bid < j0.blocks;
+    const SplitJob &j = first ? j0 : j1;
+    if (!first) bid -= j0.blocks;
+    if (j.transpose)
+        split_transpose<SMALL>(j, bid, tile);
+    else
+        split_rows<SMALL>(j, bid);
 }
 
 // ---- tcgen05 wrappers ---------------------------------------------------------------------------
@@ -313,6 +346,9 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent of the split pass: the prologue above overlapped its
+    // tail; the split operands are read only after its grid has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Output tile t of the persistent walk: batch entry b, origin (m0, n0).
     auto tile_origin = [&](int t, int &b, int &m0, int &n0) {
@@ -559,6 +595,35 @@ int sm_count(int dev) {
     return count[dev];
 }
 
+SplitJob make_job(const float *src, long long ld, long long stride, float *big, float *small,
+                  long long ldo, long long so, int rows, int cols, int batch, bool transpose,
+                  bool vec) {
+    SplitJob j;
+    j.src = src;
+    j.ld = ld;
+    j.stride = stride;
+    j.big = big;
+    j.small = small;
+    j.ldo = ldo;
+    j.so = so;
+    j.rows = rows;
+    j.cols = cols;
+    j.batch = batch;
+    j.transpose = transpose ? 1 : 0;
+    j.vec = vec ? 1 : 0;
+    if (transpose) {  // 32 x 32 tiles of the rows x cols source, per batch entry
+        j.gx = (cols + 31) / 32;
+        j.gy = (rows + 31) / 32;
+        j.blocks = static_cast<long long>(j.gx) * j.gy * batch;
+    } else {  // up to 8 CTAs of 1024 columns across a row, rows (of every batch entry) down
+        const long long nrows = static_cast<long long>(rows) * batch;
+        j.gx = static_cast<int>(std::max<long long>(1, std::min<long long>((cols + 1023) / 1024, 8)));
+        j.gy = static_cast<int>(std::min<long long>(nrows, 65535));
+        j.blocks = static_cast<long long>(j.gx) * j.gy;
+    }
+    return j;
+}
+
 template <int BN, int STAGES, int ACCS, int PRODUCTS>
 cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char **detail) {
     constexpr size_t PARTS = PRODUCTS == 3 ? 2 : 1;
@@ -609,55 +674,21 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
     {
         const bool vecA = aligned16(p.A) && p.lda % 4 == 0 && (p.batch <= 1 || p.strideA % 4 == 0);
         const bool vecB = aligned16(p.B) && p.ldb % 4 == 0 && (p.batch <= 1 || p.strideB % 4 == 0);
-        // A -> M x K (K contiguous): split in place, or split while transposing A stored K x M.
-        if (!p.transA) {
-            const long long nrows = static_cast<long long>(p.M) * p.batch;
-            const dim3 rgrid(static_cast<unsigned>(std::min<long long>((p.K + 1023) / 1024, 8)),
-                             static_cast<unsigned>(std::min<long long>(nrows, 65535)));
-            if (vecA)
-                split_rows_kernel<true, SMALL><<<rgrid, 256, 0, stream>>>(
-                    p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.M, p.K, p.batch);
-            else
-                split_rows_kernel<false, SMALL><<<rgrid, 256, 0, stream>>>(
-                    p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.M, p.K, p.batch);
-        } else {
-            dim3 grid((p.M + 31) / 32, (p.K + 31) / 32, p.batch);
-            if (vecA)
-                split_transpose_kernel<true, SMALL><<<grid, 256, 0, stream>>>(
-                    p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.K, p.M);
-            else
-                split_transpose_kernel<false, SMALL><<<grid, 256, 0, stream>>>(
-                    p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.K, p.M);
+        // A -> M x K (K contiguous): a rows job, or a transposing job when A is stored K x M.
+        // B -> N x K (K contiguous): a transposing job, or a rows job when B is stored N x K.
+        SplitJob ja = make_job(p.A, p.lda, p.strideA, a_hi, a_lo, ldk, a_elems, p.transA ? p.K : p.M,
+                               p.transA ? p.M : p.K, p.batch, p.transA, vecA);
+        SplitJob jb = make_job(p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.transB ? p.N : p.K,
+                               p.transB ? p.K : p.N, p.batch, !p.transB, vecB);
+        const long long blocks = ja.blocks + jb.blocks;
+        if (blocks > 0x7fffffffLL) {
+            *detail = "split pre-pass grid too large";
+            return cudaErrorInvalidValue;
         }
+        split_operands_kernel<SMALL><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ja, jb);
         err = cudaGetLastError();
         if (err != cudaSuccess) {
             *detail = "split kernel launch failed";
-            return err;
-        }
-        // B -> N x K (K contiguous): split while transposing B stored K x N, or in place when
-        // B is stored transposed (N x K).
-        if (!p.transB) {
-            dim3 grid((p.N + 31) / 32, (p.K + 31) / 32, p.batch);
-            if (vecB)
-                split_transpose_kernel<true, SMALL><<<grid, 256, 0, stream>>>(
-                    p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.K, p.N);
-            else
-                split_transpose_kernel<false, SMALL><<<grid, 256, 0, stream>>>(
-                    p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.K, p.N);
-        } else {
-            const long long nrows = static_cast<long long>(p.N) * p.batch;
-            const dim3 rgrid(static_cast<unsigned>(std::min<long long>((p.K + 1023) / 1024, 8)),
-                             static_cast<unsigned>(std::min<long long>(nrows, 65535)));
-            if (vecB)
-                split_rows_kernel<true, SMALL><<<rgrid, 256, 0, stream>>>(
-                    p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.N, p.K, p.batch);
-            else
-                split_rows_kernel<false, SMALL><<<rgrid, 256, 0, stream>>>(
-                    p.B, p.ldb, p.strideB, b_hi, b_lo, ldk, b_elems, p.N, p.K, p.batch);
-        }
-        err = cudaGetLastError();
-        if (err != cudaSuccess) {
-            *detail = "split-transpose kernel launch failed";
             return err;
         }
     }
@@ -693,8 +724,18 @@ cudaError_t launch_tf32x3(const SimtProblem &p, cudaStream_t stream, const char 
     }
     tp.total_tiles = static_cast<int>(tiles);
     const int grid = static_cast<int>(std::min<long long>(tiles, sms));  // one CTA per SM
-    kernel<<<grid, 192, SMEM, stream>>>(mAhi, mAlo, mBhi, mBlo, tp);
-    err = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kernel, mAhi, mAlo, mBhi, mBlo, tp);
+    if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) *detail = "3xTF32 kernel launch failed";
     return err;
 }

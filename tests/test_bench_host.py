@@ -163,4 +163,4 @@ def test_launches_per_call():
     w = {"M": 4095, "N": 3001, "K": 1537}
     assert bench.launches_per_call("simt", "sk_tma_ws_128x256_k64_s2", bench.WORKLOADS["headline"]) == 1
     assert bench.launches_per_call("simt", "packed_sk_tma_128x256_s4", w) == 3
-    assert bench.launches_per_call("3xtf32", "tf32x3_tcgen05", w) == 3
+    assert bench.launches_per_call("3xtf32", "tf32x3_tcgen05", w) == 2
