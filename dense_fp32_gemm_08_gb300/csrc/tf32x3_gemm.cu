@@ -92,7 +92,8 @@ struct SplitJob {
     int transpose;  // 0: rows job, 1: transposing job
     int vec;        // 16-byte source reads allowed
     int gx, gy;     // the job's CTA grid: rows job gx x gy; transposing job gx x gy x batch
-    long long blocks;
+    long long tiles;   // transposing job: 32 x 32 tiles in all (the CTAs loop over them)
+    long long blocks;  // CTAs of this job
 };
 
 // Rows job: rows over the grid's y dimension, columns over threads, float4 access when the
@@ -132,8 +133,8 @@ __device__ __forceinline__ void split_rows(const SplitJob &j, long long bid) {
 // float4 along n (when the source allows) and write one float4 along k of each output, so
 // both sides move 16 bytes per thread.
 template <bool SMALL>
-__device__ __forceinline__ void split_transpose(const SplitJob &j, long long bid,
-                                                float (&tile)[32][33]) {
+__device__ __forceinline__ void split_transpose_tile(const SplitJob &j, long long bid,
+                                                     float (&tile)[32][33]) {
     const int K = j.rows, N = j.cols;
     const int n0 = static_cast<int>(bid % j.gx) * 32;
     const long long rest = bid / j.gx;
@@ -184,6 +185,16 @@ __device__ __forceinline__ void split_transpose(const SplitJob &j, long long bid
                 }
             }
         }
+    }
+}
+
+// The transposing job's CTAs walk its tiles with a stride of the job's CTA count.
+template <bool SMALL>
+__device__ __forceinline__ void split_transpose(const SplitJob &j, long long bid,
+                                                float (&tile)[32][33]) {
+    for (long long t = bid; t < j.tiles; t += j.blocks) {
+        split_transpose_tile<SMALL>(j, t, tile);
+        __syncthreads();  // the tile buffer is reused by the next tile
     }
 }
 
@@ -611,14 +622,18 @@ SplitJob make_job(const float *src, long long ld, long long stride, float *big, 
     j.batch = batch;
     j.transpose = transpose ? 1 : 0;
     j.vec = vec ? 1 : 0;
+    // About 4,096 CTAs per job, each looping over several rows or tiles: CTAs of a single
+    // 4 KiB row chunk or tile spent a large share of their time starting up.
     if (transpose) {  // 32 x 32 tiles of the rows x cols source, per batch entry
         j.gx = (cols + 31) / 32;
         j.gy = (rows + 31) / 32;
-        j.blocks = static_cast<long long>(j.gx) * j.gy * batch;
+        j.tiles = static_cast<long long>(j.gx) * j.gy * batch;
+        j.blocks = std::min<long long>(j.tiles, 4096);
     } else {  // up to 8 CTAs of 1024 columns across a row, rows (of every batch entry) down
         const long long nrows = static_cast<long long>(rows) * batch;
         j.gx = static_cast<int>(std::max<long long>(1, std::min<long long>((cols + 1023) / 1024, 8)));
-        j.gy = static_cast<int>(std::min<long long>(nrows, 65535));
+        j.gy = static_cast<int>(std::max<long long>(1, std::min<long long>(nrows, 4096 / j.gx)));
+        j.tiles = 0;
         j.blocks = static_cast<long long>(j.gx) * j.gy;
     }
     return j;
