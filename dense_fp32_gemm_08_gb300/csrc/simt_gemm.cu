@@ -362,42 +362,53 @@ bool packable(const SimtProblem &p) {
     return p.batch <= 1 || (p.strideA != 0 && p.strideB != 0);
 }
 
-// ---- small problems: one warp per 64 x 64 tile, K split over CTAs ------------------------
+// ---- small problems: 64 x 64 tiles, K split over the warps of a CTA and over CTAs ------------
 //
 // For problems of a few tiles the large kernels leave most SMs idle and spend their time on
-// cold instruction fetch of a fully unrolled loop. Here each CTA is one warp computing a
-// 64 x 64 tile (the same 8 x 16 thread tile and fragment layout) over a slice of K, from a
-// two-stage cp.async ring (any alignment) and a rolled k loop. With more than one slice each
-// CTA stores its partial tile, and the CTA that finishes a tile last (an atomic count per
-// tile; nothing waits) adds the slices in slice order and applies the epilogue, so results
-// do not depend on which CTA finishes when; it then resets the count for the next call.
+// cold instruction fetch of a fully unrolled loop. Here a CTA of kSmallWarps warps computes one
+// 64 x 64 tile: each warp takes its own slice of K through its own two-stage cp.async ring (any
+// alignment), with the same 8 x 16 thread tile and fragment layout and a rolled k loop; the
+// warps then add their partial tiles through shared memory, warp w the rows [8w/W, 8(w+1)/W)
+// of every thread tile, in warp order. With more than one CTA per tile (the grid's y), each CTA
+// stores its sum, and the CTA that finishes a tile last (an atomic count per tile; nothing
+// waits) adds the CTAs' sums in CTA order and applies the epilogue, then resets the count for
+// the next call. Results do not depend on which CTA finishes when. The kernel is compiled per
+// loader form (16- or 4-byte copies of A and of B) and per epilogue form (plain or fused), so
+// each instance carries only the code it runs: at this size a cold instruction cache is a large
+// share of the time.
+
+constexpr int kSmallWarps = 4;
+constexpr int kSmallStageFloats = 64 * BK + BK * 64;  // one stage: 16 KiB
+constexpr size_t kSmallSmem = static_cast<size_t>(kSmallWarps) * 2 * kSmallStageFloats * 4;
 
 struct SmallParams {
     KParams k;
-    int split;                // K slices per tile
-    int kt_per_slice;         // 32-wide k-tiles per slice
-    float4 *partials;         // [tile][slice][32 x 32 float4]
-    unsigned int *counters;   // [tile]: slices finished
+    int ctas;                // CTAs per tile (grid y)
+    int kt_per_slice;        // 32-wide k-tiles per warp
+    float4 *partials;        // [tile][cta][32 x 32 float4]
+    unsigned int *counters;  // [tile]: CTAs finished
 };
 
-constexpr int kSmallStageFloats = 64 * BK + BK * 64;
-
-__global__ void __launch_bounds__(32) small_splitk_kernel(const SmallParams sp) {
+template <int AV, int BV, int FUSED>
+__global__ void __launch_bounds__(kSmallWarps * 32) small_splitk_kernel(const SmallParams sp) {
     const KParams &p = sp.k;
-    __shared__ __align__(16) float smem[2][kSmallStageFloats];
-    const int lane = threadIdx.x;
-    const int tile = blockIdx.x, slice = blockIdx.y;
+    extern __shared__ __align__(16) float small_smem[];  // [warp][2 stages][kSmallStageFloats]
+    __shared__ unsigned int s_last;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tile = blockIdx.x, cta = blockIdx.y;
     const int tiles_per_batch = p.tiles_m * p.tiles_n;
     const int b = tile / tiles_per_batch;
     int tm, tn;
     tile_coords(tile - b * tiles_per_batch, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     const int m0 = tm * 64, n0 = tn * 64;
     const int KT = (p.K + BK - 1) / BK;
-    const int kt0 = slice * sp.kt_per_slice;
+    const int slice = cta * kSmallWarps + warp;
+    const int kt0 = min(KT, slice * sp.kt_per_slice);
     const int kt1 = min(KT, kt0 + sp.kt_per_slice);
     const float *Ab = p.A + static_cast<long long>(b) * p.sA;
     const float *Bb = p.B + static_cast<long long>(b) * p.sB;
     const int tr = lane >> 2, tc = lane & 3;
+    float *ring = small_smem + warp * 2 * kSmallStageFloats;
 
     float2 acc[8][8];
 #pragma unroll
@@ -406,62 +417,118 @@ __global__ void __launch_bounds__(32) small_splitk_kernel(const SmallParams sp) 
         for (int j = 0; j < 8; ++j) acc[r][j] = make_float2(0.0f, 0.0f);
 
     if (kt0 < kt1)
-        cp_async_stage<64, 64, 32>(smem[0], smem[0] + 64 * BK, p, Ab, Bb, m0, n0, kt0 * BK, lane);
+        cp_async_stage<64, 64, 32, AV, BV>(ring, ring + 64 * BK, p, Ab, Bb, m0, n0, kt0 * BK, lane);
     cp_async_commit();
 #pragma unroll 1
     for (int kt = kt0; kt < kt1; ++kt) {
-        const int s = (kt - kt0) & 1;
+        float *st = ring + ((kt - kt0) & 1) * kSmallStageFloats;
+        float *nx = ring + (((kt - kt0) & 1) ^ 1) * kSmallStageFloats;
         if (kt + 1 < kt1)
-            cp_async_stage<64, 64, 32>(smem[s ^ 1], smem[s ^ 1] + 64 * BK, p, Ab, Bb, m0, n0,
-                                       (kt + 1) * BK, lane);
+            cp_async_stage<64, 64, 32, AV, BV>(nx, nx + 64 * BK, p, Ab, Bb, m0, n0, (kt + 1) * BK,
+                                               lane);
         cp_async_commit();
         cp_async_wait<1>();
         __syncwarp();  // k-tile kt landed for the whole warp
-        compute_ktile<64, kOrderHalfSnake, 1>(smem[s] + tr * BK, tr, smem[s] + 64 * BK + 4 * tc,
-                                              acc);
-        __syncwarp();  // stage s is free for the load two k-tiles ahead
+        compute_ktile<64, kOrderHalfSnake, 1>(st + tr * BK, tr, st + 64 * BK + 4 * tc, acc);
+        __syncwarp();  // the stage is free for the load two k-tiles ahead
     }
     cp_async_wait<0>();
+    __syncwarp();
 
-    float *Cb = p.C + static_cast<long long>(b) * p.sC;
-    if (sp.split == 1) {
-        epilogue(p, Cb, m0 + tr, n0 + 4 * tc, acc);
-        return;
-    }
-    float4 *mine = sp.partials + (static_cast<size_t>(tile) * sp.split + slice) * 1024;
+    // This warp's partial tile into its own ring (16 KiB: one float4 per (j, lane)).
+    float4 *part = reinterpret_cast<float4 *>(ring);
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         const int r = j >> 2, q = j & 3;
-        mine[j * 32 + lane] = make_float4(acc[r][2 * q].x, acc[r][2 * q].y, acc[r][2 * q + 1].x,
+        part[j * 32 + lane] = make_float4(acc[r][2 * q].x, acc[r][2 * q].y, acc[r][2 * q + 1].x,
                                           acc[r][2 * q + 1].y);
     }
-    __threadfence();
-    __syncwarp();
-    unsigned int done = 0;
-    if (lane == 0) done = atomicAdd(&sp.counters[tile], 1u);
-    done = __shfl_sync(0xffffffffu, done, 0);
-    if (done != static_cast<unsigned int>(sp.split - 1)) return;  // not the last slice to finish
-    __threadfence();
-    const float4 *base = sp.partials + static_cast<size_t>(tile) * sp.split * 1024;
-#pragma unroll 1
-    for (int sl = 0; sl < sp.split; ++sl) {
+    __syncthreads();  // every warp's partial tile is in shared memory
+
+    // Warp w adds rows [r0, r1) of the thread tiles over the warps, in warp order.
+    const int r0 = warp * 8 / kSmallWarps, r1 = (warp + 1) * 8 / kSmallWarps;
+    const float4 *parts = reinterpret_cast<const float4 *>(small_smem);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int r = j >> 2, q = j & 3;
-            const float4 v = __ldcg(base + static_cast<size_t>(sl) * 1024 + j * 32 + lane);
-            if (sl == 0) {
-                acc[r][2 * q] = make_float2(v.x, v.y);
-                acc[r][2 * q + 1] = make_float2(v.z, v.w);
-            } else {
-                acc[r][2 * q].x += v.x;
-                acc[r][2 * q].y += v.y;
-                acc[r][2 * q + 1].x += v.z;
-                acc[r][2 * q + 1].y += v.w;
+    for (int r = 0; r < 8; ++r) {
+        if (r < r0 || r >= r1) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = r * 4 + q;
+            float4 sum = parts[j * 32 + lane];
+#pragma unroll
+            for (int w = 1; w < kSmallWarps; ++w) {
+                const float4 v = parts[static_cast<size_t>(w) * 2 * kSmallStageFloats / 4 + j * 32 + lane];
+                sum.x += v.x;
+                sum.y += v.y;
+                sum.z += v.z;
+                sum.w += v.w;
+            }
+            acc[r][2 * q] = make_float2(sum.x, sum.y);
+            acc[r][2 * q + 1] = make_float2(sum.z, sum.w);
+        }
+    }
+
+    float *Cb = p.C + static_cast<long long>(b) * p.sC;
+    if (sp.ctas == 1) {
+        epilogue<1, FUSED>(p, Cb, m0 + tr, n0 + 4 * tc, acc, r0, r1);
+        return;
+    }
+    // Several CTAs per tile: store this CTA's sums; the last CTA to finish adds them all.
+    float4 *mine = sp.partials + (static_cast<size_t>(tile) * sp.ctas + cta) * 1024;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        if (r < r0 || r >= r1) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            mine[(r * 4 + q) * 32 + lane] = make_float4(acc[r][2 * q].x, acc[r][2 * q].y,
+                                                        acc[r][2 * q + 1].x, acc[r][2 * q + 1].y);
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        s_last = atomicAdd(&sp.counters[tile], 1u) == static_cast<unsigned int>(sp.ctas - 1);
+    __syncthreads();
+    if (!s_last) return;  // not the last CTA of this tile to finish
+    __threadfence();
+    const float4 *base = sp.partials + static_cast<size_t>(tile) * sp.ctas * 1024;
+#pragma unroll 1
+    for (int c = 0; c < sp.ctas; ++c) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            if (r < r0 || r >= r1) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = __ldcg(base + static_cast<size_t>(c) * 1024 + (r * 4 + q) * 32 + lane);
+                if (c == 0) {
+                    acc[r][2 * q] = make_float2(v.x, v.y);
+                    acc[r][2 * q + 1] = make_float2(v.z, v.w);
+                } else {
+                    acc[r][2 * q].x += v.x;
+                    acc[r][2 * q].y += v.y;
+                    acc[r][2 * q + 1].x += v.z;
+                    acc[r][2 * q + 1].y += v.w;
+                }
             }
         }
     }
-    if (lane == 0) sp.counters[tile] = 0u;  // ready for the next launch on this stream
-    epilogue(p, Cb, m0 + tr, n0 + 4 * tc, acc);
+    if (threadIdx.x == 0) sp.counters[tile] = 0u;  // ready for the next launch on this stream
+    epilogue<1, FUSED>(p, Cb, m0 + tr, n0 + 4 * tc, acc, r0, r1);
+}
+
+// The instance for the problem's loader and epilogue forms, with its shared-memory limit set
+// once per device.
+template <int AV, int BV, int FUSED>
+cudaError_t launch_small_instance(int dev, const SmallParams &sp, dim3 grid, cudaStream_t stream) {
+    auto kernel = small_splitk_kernel<AV, BV, FUSED>;
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t attr_err[kMaxDevices];
+    std::call_once(once[dev], [&] {
+        attr_err[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmallSmem));
+    });
+    if (attr_err[dev] != cudaSuccess) return attr_err[dev];
+    kernel<<<grid, kSmallWarps * 32, kSmallSmem, stream>>>(sp);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_small_splitk(const SimtProblem &p, cudaStream_t stream, const char **detail) {
@@ -470,6 +537,10 @@ cudaError_t launch_small_splitk(const SimtProblem &p, cudaStream_t stream, const
     if (err != cudaSuccess) {
         *detail = "cudaGetDevice failed";
         return err;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        *detail = "device ordinal above the library's limit";
+        return cudaErrorInvalidDevice;
     }
     SmallParams sp;
     KParams &kp = sp.k;
@@ -501,23 +572,22 @@ cudaError_t launch_small_splitk(const SimtProblem &p, cudaStream_t stream, const
         *detail = "too many output tiles for the split-K grid";
         return cudaErrorInvalidValue;
     }
-    // Slices: enough one-warp CTAs for about four per SM, at most 16 and at most one per
-    // 32-wide k-tile; then no empty slice.
-    const long long KT = (p.K + BK - 1) / BK;
+    // Warp slices of K: at most one per 32-wide k-tile, and CTAs per tile (one CTA per SM, its
+    // shared memory is 128 KiB) as many as the SMs hold next to the other tiles, at most 16.
+    const long long KT = std::max<long long>(1, (p.K + BK - 1) / BK);
     const int sms = std::max(1, device_sms(dev));
-    long long split = (4LL * sms + tiles - 1) / tiles;
-    split = std::min<long long>(std::min<long long>(split, 16), std::max<long long>(KT, 1));
-    if (split < 1) split = 1;
-    const long long per = (KT + split - 1) / split;
-    split = per > 0 ? (KT + per - 1) / per : 1;
-    if (split < 1) split = 1;
-    sp.split = static_cast<int>(split);
-    sp.kt_per_slice = static_cast<int>(per > 0 ? per : 1);
+    long long ctas = std::max<long long>(1, std::min<long long>(sms / tiles, 16));
+    ctas = std::min<long long>(ctas, (KT + kSmallWarps - 1) / kSmallWarps);
+    const long long per = (KT + ctas * kSmallWarps - 1) / (ctas * kSmallWarps);
+    ctas = (KT + per * kSmallWarps - 1) / (per * kSmallWarps);  // no CTA without k-tiles
+    if (ctas < 1) ctas = 1;
+    sp.ctas = static_cast<int>(ctas);
+    sp.kt_per_slice = static_cast<int>(per);
     sp.partials = nullptr;
     sp.counters = nullptr;
-    if (split > 1) {
+    if (ctas > 1) {
         // The counts live in their own allocation: zeroed whenever it is (re)allocated, and
-        // left at zero by every launch (the last slice of each tile resets its count), so any
+        // left at zero by every launch (the last CTA of each tile resets its count), so any
         // later launch on this stream, of any tile count that fits, starts from zeros.
         float *cnt = nullptr, *ws = nullptr;
         bool fresh = false;
@@ -526,7 +596,7 @@ cudaError_t launch_small_splitk(const SimtProblem &p, cudaStream_t stream, const
         if (err == cudaSuccess && fresh) err = cudaMemsetAsync(cnt, 0, count_bytes, stream);
         if (err == cudaSuccess)
             err = pack_workspace(dev, stream, kSlotSplitK,
-                                 static_cast<size_t>(tiles) * split * 1024 * sizeof(float4), &ws);
+                                 static_cast<size_t>(tiles) * ctas * 1024 * sizeof(float4), &ws);
         if (err != cudaSuccess) {
             *detail = "split-K workspace allocation failed";
             return err;
@@ -534,10 +604,20 @@ cudaError_t launch_small_splitk(const SimtProblem &p, cudaStream_t stream, const
         sp.counters = reinterpret_cast<unsigned int *>(cnt);
         sp.partials = reinterpret_cast<float4 *>(ws);
     }
-    small_splitk_kernel<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(split)), 32, 0,
-                          stream>>>(sp);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) *detail = "kernel launch failed";
+    const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(ctas));
+    const bool fused = p.bias != nullptr || p.act != kActNone;
+    const int form = (kp.a_vec4 ? 4 : 0) + (kp.b_vec4 ? 2 : 0) + (fused ? 1 : 0);
+    switch (form) {
+        case 0: err = launch_small_instance<0, 0, 0>(dev, sp, grid, stream); break;
+        case 1: err = launch_small_instance<0, 0, 1>(dev, sp, grid, stream); break;
+        case 2: err = launch_small_instance<0, 1, 0>(dev, sp, grid, stream); break;
+        case 3: err = launch_small_instance<0, 1, 1>(dev, sp, grid, stream); break;
+        case 4: err = launch_small_instance<1, 0, 0>(dev, sp, grid, stream); break;
+        case 5: err = launch_small_instance<1, 0, 1>(dev, sp, grid, stream); break;
+        case 6: err = launch_small_instance<1, 1, 0>(dev, sp, grid, stream); break;
+        default: err = launch_small_instance<1, 1, 1>(dev, sp, grid, stream); break;
+    }
+    if (err != cudaSuccess) *detail = "small split-K kernel launch failed";
     return err;
 }
 

@@ -177,11 +177,13 @@ __device__ __forceinline__ void compute_ktile(const float *__restrict__ a_base, 
 }
 
 // cp.async fill of one stage: A tile (BM x 32, swizzled rows) and B tile (32 x BN).
-template <int BM, int BN, int THREADS>
+// AV / BV: 1 or 0 fixes at compile time whether A / B take 16-byte copies (only that form's
+// code is emitted); -1 reads p.a_vec4 / p.b_vec4.
+template <int BM, int BN, int THREADS, int AV = -1, int BV = -1>
 __device__ __forceinline__ void cp_async_stage(float *sA, float *sB, const KParams &p,
                                                const float *Ab, const float *Bb, int m0, int n0,
                                                int k0, int tid) {
-    if (p.a_vec4) {
+    if (AV < 0 ? p.a_vec4 != 0 : AV != 0) {
 #pragma unroll 4
         for (int c = tid; c < BM * (BK / 4); c += THREADS) {
             const int m = c >> 3, kc = c & 7;
@@ -208,7 +210,7 @@ __device__ __forceinline__ void cp_async_stage(float *sA, float *sB, const KPara
             cp_async_4(smem_addr(sA + m * BK + (((k >> 2) ^ (m & 7)) << 2) + (k & 3)), src, bytes);
         }
     }
-    if (p.b_vec4) {
+    if (BV < 0 ? p.b_vec4 != 0 : BV != 0) {
 #pragma unroll 4
         for (int c = tid; c < BK * (BN / 4); c += THREADS) {
             const int k = c / (BN / 4), nc = c % (BN / 4);
@@ -290,14 +292,15 @@ __device__ __forceinline__ void store_c4(const KParams &p, float *crow, int gn, 
 }
 
 // CHUNKS: 4-column chunks of C loaded per round trip by the plain form (2, or 1 where the
-// kernel has no registers to spare).
-template <int CHUNKS = 2>
+// kernel has no registers to spare). FUSED: 1 or 0 fixes the form at compile time (only its code
+// is emitted); -1 decides from p.bias and p.act.
+template <int CHUNKS = 2, int FUSED = -1>
 __device__ __forceinline__ void epilogue(const KParams &p, float *Cb, int row0, int col0,
                                          const float2 (&acc)[8][8], int r_begin = 0,
                                          int r_end = 8) {
     static_assert(CHUNKS == 1 || CHUNKS == 2, "one or two chunks per round trip");
     const float alpha = p.alpha, beta = p.beta;
-    const bool fused = p.bias != nullptr || p.act != kActNone;
+    const bool fused = FUSED < 0 ? (p.bias != nullptr || p.act != kActNone) : FUSED != 0;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         const int gm = row0 + 8 * r;
