@@ -379,6 +379,50 @@ def result_check(w, A, B, C, rows, want, got_full):
             "what": "result of the timed call against the oracle rows of the cpu_baseline sample"}
 
 
+def oracle_sizes(rows_cap_s: float = 0.5, sizes=(256, 1024, 2048, 8192, 16384), full_up_to=2048,
+                 single_core_up_to=1024):
+    """The oracle on the square sizes of the sweep, on the machine's host cores: 256^3 to 2048^3 in
+    full (256^3 and 1024^3 also on one core), 8192^3 and 16384^3 on a row sample sized for
+    about `rows_cap_s` seconds, extrapolated to the full size and labelled so. Inputs are drawn
+    from numpy's seeded generator (uniform [-1, 1)); the oracle's time does not depend on the
+    values."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(0)
+    full = oracle.max_threads()
+    out = []
+    for n in sizes:
+        A = (rng.random((n, n), dtype=np.float32) * 2 - 1)
+        B = (rng.random((n, n), dtype=np.float32) * 2 - 1)
+        modes = [full] + ([1] if n <= single_core_up_to else [])
+        for threads in modes:
+            oracle.set_threads(threads)
+            try:
+                if n <= full_up_to:
+                    t0 = time.perf_counter()
+                    oracle.sgemm(n, n, n, 1.0, A, n, B, n, 0.0, None, n)
+                    dt, rows = time.perf_counter() - t0, n
+                else:
+                    probe = np.arange(min(n, 2 * threads))
+                    t0 = time.perf_counter()
+                    oracle.sgemm(n, n, n, 1.0, A, n, B, n, 0.0, None, n, rows=probe)
+                    per_row = (time.perf_counter() - t0) / len(probe)
+                    rows = int(min(n, max(len(probe), rows_cap_s / max(per_row, 1e-9))))
+                    sample = np.sort(rng.choice(n, size=rows, replace=False))
+                    t0 = time.perf_counter()
+                    oracle.sgemm(n, n, n, 1.0, A, n, B, n, 0.0, None, n, rows=sample)
+                    dt = time.perf_counter() - t0
+            finally:
+                oracle.set_threads(full)
+            gf = 2.0 * rows * n * n / dt / 1e9
+            out.append({"n": n, "cores": threads, "gflops": round(gf, 3),
+                        "seconds_full": round(2.0 * n ** 3 / (gf * 1e9), 2),
+                        "how": "full" if rows == n else
+                               f"extrapolated from {rows} of {n} rows (all columns, full K)"})
+        del A, B
+    return out
+
+
 def oracle_sample(w, target_s: float, A, B, C, threads: int | None = None, result=None):
     """Times the oracle on a row sample sized for about `target_s` seconds, on `threads`
     OpenMP threads (default: all). Returns (gflops, seconds, rows, threads, check), where
@@ -623,6 +667,8 @@ def run_ours(args):
             "value": round(gf1, 3), "unit": UNIT, "cores": 1,
             "sample": f"{n1} of {M} result rows (all N columns, full K), {dt1:.1f} s"}
         line["check"] = check
+        if not args.no_oracle_sizes:
+            line["cpu_baseline"]["sizes"] = oracle_sizes()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -869,6 +915,8 @@ def parse(argv=None):
     ap.add_argument("--no-sustained", action="store_true",
                     help="skip the one-second sustained loop after the timed steps")
     ap.add_argument("--sustain-s", type=float, default=1.0)
+    ap.add_argument("--no-oracle-sizes", action="store_true",
+                    help="skip timing the oracle on the square sizes of the sweep")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cublas-context", action="store_true",

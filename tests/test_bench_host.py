@@ -164,3 +164,15 @@ def test_launches_per_call():
     assert bench.launches_per_call("simt", "sk_tma_ws_128x256_k64_s2", bench.WORKLOADS["headline"]) == 1
     assert bench.launches_per_call("simt", "packed_sk_tma_128x256_s4", w) == 3
     assert bench.launches_per_call("3xtf32", "tf32x3_tcgen05", w) == 2
+
+
+def test_oracle_sizes_are_bounded_and_labelled():
+    # Timing the oracle on square sizes: the small ones in full (and on one core), the large
+    # ones on a row sample, extrapolated and labelled (small sizes keep this test quick).
+    out = bench.oracle_sizes(rows_cap_s=1e-6, sizes=(32, 64, 160), full_up_to=64,
+                             single_core_up_to=32)
+    assert sorted({r["n"] for r in out}) == [32, 64, 160]
+    for r in out:
+        assert r["gflops"] > 0 and r["cores"] >= 1 and r["seconds_full"] >= 0
+        assert (r["how"] == "full") == (r["n"] <= 64)
+    assert [r["cores"] for r in out if r["n"] == 32][-1] == 1
