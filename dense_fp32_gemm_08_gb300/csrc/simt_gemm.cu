@@ -572,12 +572,18 @@ cudaError_t launch_small_splitk(const SimtProblem &p, cudaStream_t stream, const
         *detail = "too many output tiles for the split-K grid";
         return cudaErrorInvalidValue;
     }
-    // Warp slices of K: at most one per 32-wide k-tile, and CTAs per tile (one CTA per SM, its
-    // shared memory is 128 KiB) as many as the SMs hold next to the other tiles, at most 16.
+    // Warp slices of K: a CTA's warps share a tile's k-tiles; more CTAs per tile (one CTA per
+    // SM, its shared memory is 128 KiB) only once a warp would run more than kSmallKtPerWarp
+    // k-tiles, as many as the SMs hold next to the other tiles, at most 16. A second CTA costs a
+    // pass of partial sums through global memory, measured between one and two k-tiles of a
+    // warp (256^3: one CTA per tile 15.9 us against two 17.2 us; 512^3: two CTAs 20.8 us
+    // against one 22.8 us).
+    constexpr long long kSmallKtPerWarp = 2;
     const long long KT = std::max<long long>(1, (p.K + BK - 1) / BK);
     const int sms = std::max(1, device_sms(dev));
     long long ctas = std::max<long long>(1, std::min<long long>(sms / tiles, 16));
-    ctas = std::min<long long>(ctas, (KT + kSmallWarps - 1) / kSmallWarps);
+    ctas = std::min<long long>(ctas, (KT + kSmallWarps * kSmallKtPerWarp - 1) /
+                                         (kSmallWarps * kSmallKtPerWarp));
     const long long per = (KT + ctas * kSmallWarps - 1) / (ctas * kSmallWarps);
     ctas = (KT + per * kSmallWarps - 1) / (per * kSmallWarps);  // no CTA without k-tiles
     if (ctas < 1) ctas = 1;
