@@ -37,7 +37,9 @@ def main(argv=None):
     result = {"device": torch.cuda.get_device_name(0),
               "sms": torch.cuda.get_device_properties(0).multi_processor_count,
               "when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()), "classes": {}}
-    if args.classes and Path(args.out).exists():
+    if args.classes:
+        if not Path(args.out).exists():
+            ap.error(f"--classes re-measures part of an existing table, and {args.out} is missing")
         kept = json.loads(Path(args.out).read_text())["classes"]
         result["classes"] = {c: v for c, v in kept.items() if c not in args.classes}
     try:
