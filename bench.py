@@ -41,6 +41,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -284,15 +285,24 @@ KERNEL_SOURCES = {
 }
 
 
+def code_of(text: str) -> str:
+    """A C/CUDA source without its comments and with runs of whitespace collapsed: what the
+    compiler sees, so that editing a comment does not mark ncu figures stale."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash(path: str = "simt") -> str:
-    """Hash of the source files that define a path's kernels (ncu figures go stale with them)."""
+    """Hash of the code of the source files that define a path's kernels (ncu figures go
+    stale with it)."""
     h = hashlib.sha256()
     csrc = ROOT / "dense_fp32_gemm_08_gb300" / "csrc"
     for name in KERNEL_SOURCES[path]:
         p = csrc / name
         if p.exists():
             h.update(name.encode())
-            h.update(p.read_bytes())
+            h.update(code_of(p.read_text()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,6 +1,6 @@
 // tf32x3_gemm.cu: C = alpha * (A . B) + beta * C on the tcgen05 tensor cores, fp32 emulated by
-// three TF32 products (the "3xTF32" split; the pages name tensor cores only as the "different
-// vehicle" above the SIMT ladder, "GEMM scrapbook", closing remarks).
+// three TF32 products (the published "3xTF32" split; the pages mention tensor cores only in
+// passing, as the way past the SIMT ladder, "GEMM scrapbook", closing remarks).
 //
 // Split. Every operand value x becomes big = tf32_rna(x) and small = tf32_rna(x - big); big
 // has the low 13 mantissa bits clear, x - big is exact in fp32, and big.big + big.small +

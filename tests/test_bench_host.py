@@ -47,16 +47,24 @@ def test_ncu_traffic_requires_matching_source(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", tmp_path)
     (tmp_path / "profiles").mkdir()
     (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc").mkdir(parents=True)
-    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "simt_gemm.cu").write_text("// v1")
+    src = tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "simt_gemm.cu"
+    src.write_text("// v1\nint f() { return 1; }\n")
     h = bench.source_hash()
     data = {"kern@headline": {"dram_bytes_per_launch": 123, "source_hash": h}}
     (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(data))
     assert bench.ncu_traffic("kern", "headline") == 123
-    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "tf32x3_gemm.cu").write_text("// other")
+    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "tf32x3_gemm.cu").write_text("int g;")
     assert bench.ncu_traffic("kern", "headline") == 123  # another path's file: still valid
-    (tmp_path / "dense_fp32_gemm_08_gb300" / "csrc" / "simt_gemm.cu").write_text("// v2")
-    assert bench.ncu_traffic("kern", "headline") is None
+    src.write_text("/* reworded */\nint f()  {\n  return 1;  // same code\n}\n")
+    assert bench.ncu_traffic("kern", "headline") == 123  # comments and layout only: still valid
+    src.write_text("// v1\nint f() { return 2; }\n")
+    assert bench.ncu_traffic("kern", "headline") is None  # the code changed
     assert bench.ncu_traffic("other", "headline") is None
+
+
+def test_code_of_drops_comments_only():
+    assert bench.code_of("a = 1; // x\n/* y\n z */ b  =\n 2;") == "a = 1; b = 2;"
+    assert bench.code_of("x = 1;") != bench.code_of("x = 2;")
 
 
 def test_oracle_timer_counts_rows():
