@@ -185,6 +185,11 @@ bool packable(const SimtProblem &p);
 cudaError_t launch_small_splitk(const SimtProblem &p, cudaStream_t stream, const char **detail);
 cudaError_t launch_packed(int inner, const SimtProblem &p, cudaStream_t stream,
                           const char **detail);
+bool stage_c(int id, const SimtProblem &p);
+cudaError_t launch_staged_c(int id, const SimtProblem &p, cudaStream_t stream,
+                            const char **detail);
+cudaError_t launch_config(int id, const SimtProblem &p, cudaStream_t stream,
+                          const char **detail);
 
 }  // namespace
 
@@ -211,6 +216,18 @@ bool simt_config_supports(int id, const SimtProblem &p) {
 }
 
 cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const char **detail) {
+    if (id < 0 || id >= kNumConfigs) {
+        *detail = "unknown SIMT configuration";
+        return cudaErrorInvalidValue;
+    }
+    return stage_c(id, p) ? launch_staged_c(id, p, stream, detail)
+                          : launch_config(id, p, stream, detail);
+}
+
+namespace {
+
+cudaError_t launch_config(int id, const SimtProblem &p, cudaStream_t stream,
+                          const char **detail) {
     switch (id) {
         case 0: case 1: case 2: return simt_launch_dp(id, p, stream, detail);
         case 3: case 4: return simt_launch_dpcp(id, p, stream, detail);
@@ -229,6 +246,8 @@ cudaError_t simt_launch(int id, const SimtProblem &p, cudaStream_t stream, const
         default: *detail = "unknown SIMT configuration"; return cudaErrorInvalidValue;
     }
 }
+
+}  // namespace
 
 cudaError_t release_workspaces() {
     std::lock_guard<std::mutex> lock(g_ws_mutex);
@@ -325,6 +344,7 @@ constexpr int kSlotTransposed = 0;
 constexpr int kSlotRealigned = 1;
 constexpr int kSlotSplitK = 2;        // split-K partial tiles
 constexpr int kSlotSplitKCount = 3;   // split-K per-tile counts (zero between launches)
+constexpr int kSlotStagedC = 4;       // the product of a staged-C call (stage_c)
 
 // *fresh (when given) reports a new allocation, whose contents are undefined.
 cudaError_t pack_workspace(int dev, cudaStream_t stream, int slot, size_t bytes, float **out,
@@ -677,7 +697,88 @@ cudaError_t launch_packed(int inner, const SimtProblem &p, cudaStream_t stream,
         *detail = "operands not readable by TMA after repacking";
         return cudaErrorInvalidValue;
     }
-    return simt_launch(inner, q, stream, detail);
+    return launch_config(inner, q, stream, detail);
+}
+
+// ---- C that the epilogue cannot read with 16-byte loads, beta != 0 ------------------------------
+//
+// With an unaligned C (odd ldc, say) the tile epilogue reads C with 4-byte loads, one memory
+// round trip per few values, while its warps wait (4095 x 3001 x 1537: 61 us of 742). For
+// large problems the product is computed instead into an aligned scratch D with the beta = 0
+// epilogue (alpha = 1, no bias or activation: D holds the fp32 accumulators as they are), and a
+// streaming pass applies the caller's epilogue to C: the same expression on the same fp32
+// values, so the result is bit-identical to the in-kernel epilogue.
+constexpr long long kStageCMinElems = 1LL << 22;
+
+// Rows over the grid's y dimension (batch entries stacked), four consecutive columns per
+// thread: one 16-byte load of D (its leading dimension is a multiple of 4; a row's last group
+// may read padding, which is allocated and unused), the C values loaded before any store.
+__global__ void apply_staged_c_kernel(const float *__restrict__ D, long long ldd, long long sd,
+                                      float *__restrict__ C, long long ldc, long long sc,
+                                      int rows, int cols, int batch, float alpha, float beta,
+                                      const float *__restrict__ bias, int act) {
+    const long long nrows = static_cast<long long>(rows) * batch;
+    const bool fused = bias != nullptr || act != kActNone;
+    for (long long gr = blockIdx.y; gr < nrows; gr += gridDim.y) {
+        const long long b = gr / rows, r = gr - b * rows;
+        const float *d = D + b * sd + r * ldd;
+        float *c = C + b * sc + r * ldc;
+        for (int j = 4 * (blockIdx.x * blockDim.x + threadIdx.x); j < cols;
+             j += 4 * gridDim.x * blockDim.x) {
+            const float4 v4 = __ldcs(reinterpret_cast<const float4 *>(d + j));
+            const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+            const int n = cols - j < 4 ? cols - j : 4;
+            float cv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (e < n) cv[e] = c[j + e];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (e < n)
+                    c[j + e] = fused ? epilogue_apply(v[e], alpha, beta, bias, j + e, act, cv[e])
+                                     : fmaf(alpha, v[e], beta * cv[e]);
+        }
+    }
+}
+
+bool stage_c(int id, const SimtProblem &p) {
+    if (p.beta == 0.0f || operand_vec4(p.C, p.ldc, p.strideC, p.batch)) return false;
+    if (id == 10 || id == 11 || id == 19) return false;  // skinny and small-problem kernels
+    return static_cast<long long>(p.M) * p.N * p.batch >= kStageCMinElems;
+}
+
+cudaError_t launch_staged_c(int id, const SimtProblem &p, cudaStream_t stream,
+                            const char **detail) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) {
+        *detail = "cudaGetDevice failed";
+        return err;
+    }
+    const long long ldd = (static_cast<long long>(p.N) + 3) / 4 * 4;
+    const long long elems = static_cast<long long>(p.M) * ldd;
+    float *D = nullptr;
+    err = pack_workspace(dev, stream, kSlotStagedC, static_cast<size_t>(elems) * p.batch * 4, &D);
+    if (err != cudaSuccess) {
+        *detail = "staged-C workspace allocation failed";
+        return err;
+    }
+    SimtProblem q = p;
+    q.C = D;
+    q.ldc = ldd;
+    q.strideC = p.batch > 1 ? elems : 0;
+    q.alpha = 1.0f;
+    q.beta = 0.0f;
+    q.bias = nullptr;
+    q.act = kActNone;
+    err = launch_config(id, q, stream, detail);
+    if (err != cudaSuccess) return err;
+    apply_staged_c_kernel<<<rows_grid(static_cast<long long>(p.M) * p.batch, p.N), 256, 0,
+                            stream>>>(D, ldd, elems, p.C, p.ldc, p.strideC, p.M, p.N, p.batch,
+                                      p.alpha, p.beta, p.bias, p.act);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) *detail = "staged-C epilogue launch failed";
+    return err;
 }
 
 }  // namespace

@@ -113,6 +113,17 @@ def test_fused_llm_ffn_up_gelu(sgemm_lib):
     _run(sgemm_lib, 16384, 14336, 4096, 1.0, 0.0, "gelu", True, seed=0, rows=rows)
 
 
+@pytest.mark.parametrize("act", ["relu", "gelu", "silu"])
+def test_fused_unaligned_c_staged(sgemm_lib, act):
+    # ldc = 2049 (odd) and beta != 0 over 4.2 M outputs: the product is staged in an aligned
+    # scratch and the bias, activation and beta * C are applied by a separate pass
+    rows = sorted({0, 2048, *range(1920, 2049, 41), *np.random.default_rng(1).integers(0, 2049, 8).tolist()})
+    _run(sgemm_lib, 2049, 2049, 300, 0.7, -1.3, act, True, seed=4, rows=rows)
+    got, ref = _run(sgemm_lib, 2049, 2049, 300, 1.0, 2.0, "relu" if act == "relu" else "none",
+                    True, seed=5, dist="small_int", rows=rows)
+    assert np.array_equal(got, ref)
+
+
 def test_fused_strided_batched(sgemm_lib):
     sg = sgemm_lib
     M, N, K, batch = 200, 160, 96, 3

@@ -338,6 +338,42 @@ def test_strided_batched_broadcast_and_padding(sg):
     _batched(sg, M, N, K, batch, M * K + 12, 0, M * N + 8, 1.0, 0.5, sg.sgemm_strided_batched)
 
 
+# ---- C without 16-byte rows and beta != 0: the product staged in an aligned scratch ------------
+# (problems of at least 2^22 outputs; the pass that applies alpha, beta, bias and the activation
+# reads C with 4-byte loads and must leave every value outside the M x N window untouched)
+
+@pytest.mark.parametrize("name", [None, "dp_tma_128x128_s3", "dp_cpasync_128x256_s4",
+                                  "sk_tma_ws_256x128_k64_s2", "sk_tma_ws_128x128_s3",
+                                  "ck_tma_128x256_k64_s2", "packed_sk_tma_256x128_k64_s2"])
+def test_unaligned_c_beta_staged(sg, name):
+    sg.sgemm_force_config(_config_id(sg, name))
+    try:
+        # odd ldc (A and B stay TMA-readable, so the forced TMA kernels run)
+        _check(Case(2049, 2052, 516, 0.7, -1.3, "normal", seed=31, ldc_pad=1,
+                    rows=sample_rows(2049, n=12)), sg)
+        # C's base 4 bytes past a 16-byte boundary; small integers: bit-exact
+        got, ref = _check(Case(2048, 2052, 260, 1.0, -2.0, "small_int", seed=32, c_off=1,
+                               rows=sample_rows(2048, n=12)), sg)
+        assert np.array_equal(got, ref)
+    finally:
+        sg.sgemm_force_config(-1)
+
+
+@pytest.mark.parametrize("M,N,K", [(4095, 3001, 1537), (2051, 2049, 300)])
+def test_unaligned_c_beta_staged_exact(sg, M, N, K):
+    got, ref = _check(Case(M, N, K, 1.0, 3.0, "small_int", seed=33, rows=sample_rows(M, n=16)),
+                      sg)
+    assert np.array_equal(got, ref)
+
+
+def test_unaligned_c_beta_staged_batched(sg):
+    # 2 x 1025 x 2049 outputs, ldc = 2049, strideC odd
+    M, N, K, batch = 1025, 2049, 64, 2
+    _batched(sg, M, N, K, batch, M * K, K * N, M * N + 1, 0.7, -1.3, sg.sgemm_strided_batched)
+    _batched(sg, M, N, K, batch, M * K, K * N, M * N + 1, 1.0, 1.0, sg.sgemm_strided_batched,
+             exact=True)
+
+
 # ---- device status ---------------------------------------------------------------------------
 
 def test_device_status_clean(sg):
