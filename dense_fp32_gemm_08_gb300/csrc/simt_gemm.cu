@@ -299,27 +299,51 @@ cudaError_t simt_selftest_wait(int which, cudaStream_t stream) {
 // is cheaper than feeding every k-tile through 4-byte cp.async copies.
 namespace {
 
-// Rows run over the grid's y dimension (batch entries stacked), columns over threads, four
-// consecutive columns per thread: four scalar loads from the unaligned source row (a warp's
-// loads still cover 512 contiguous bytes) and one 16-byte store into the aligned copy, whose
-// leading dimension is a multiple of 4 with a 16-byte aligned base.
-__global__ void pack_rows_kernel(const float *__restrict__ src, long long lds, long long ss,
-                                 float *__restrict__ dst, long long ldd, long long sd, int rows,
-                                 int cols, int batch) {
+// One operand to copy: rows x cols values (leading dimension lds, batch stride ss) into dst
+// (leading dimension ldd, a multiple of 4, 16-byte aligned base; batch stride sd), by a grid of
+// gx x gy CTAs (gx across a row, gy down the rows of every batch entry).
+struct PackJob {
+    const float *src;
+    long long lds, ss;
+    float *dst;
+    long long ldd, sd;
+    int rows, cols;
+    int gx, gy;
+};
+
+PackJob pack_job(const float *src, long long lds, long long ss, float *dst, long long ldd,
+                 long long sd, int rows, int cols, int batch) {
     const long long nrows = static_cast<long long>(rows) * batch;
-    const int c4 = cols & ~3;
-    for (long long gr = blockIdx.y; gr < nrows; gr += gridDim.y) {
-        const long long b = gr / rows, r = gr - b * rows;
-        const float *s = src + b * ss + r * lds;
-        float *d = dst + b * sd + r * ldd;
-        for (int c = 4 * (blockIdx.x * blockDim.x + threadIdx.x); c < c4;
-             c += 4 * gridDim.x * blockDim.x) {
+    const int gx = static_cast<int>(std::max<long long>(1, std::min<long long>((cols + 1023) / 1024, 8)));
+    const int gy = static_cast<int>(std::max<long long>(1, std::min<long long>(nrows, 65535)));
+    return {src, lds, ss, dst, ldd, sd, rows, cols, gx, gy};
+}
+
+// Both operands in one launch, so that the two copies stream at once: CTAs [0, gx0 * gy0) copy
+// the first job, the rest the second. Rows run down the job's gy (batch entries stacked),
+// columns across its gx, four consecutive columns per thread: four scalar loads from the
+// unaligned source row (a warp's loads still cover 512 contiguous bytes) and one 16-byte store
+// into the aligned copy.
+__global__ void pack_rows_kernel(const PackJob j0, const PackJob j1, int batch) {
+    long long bid = blockIdx.x;
+    const long long blocks0 = static_cast<long long>(j0.gx) * j0.gy;
+    const bool first = bid < blocks0;
+    const PackJob &j = first ? j0 : j1;
+    if (!first) bid -= blocks0;
+    const int bx = static_cast<int>(bid % j.gx);
+    const long long by = bid / j.gx;
+    const long long nrows = static_cast<long long>(j.rows) * batch;
+    const int c4 = j.cols & ~3;
+    for (long long gr = by; gr < nrows; gr += j.gy) {
+        const long long b = gr / j.rows, r = gr - b * j.rows;
+        const float *s = j.src + b * j.ss + r * j.lds;
+        float *d = j.dst + b * j.sd + r * j.ldd;
+        for (int c = 4 * (bx * blockDim.x + threadIdx.x); c < c4; c += 4 * j.gx * blockDim.x) {
             const float4 v = make_float4(__ldcs(s + c), __ldcs(s + c + 1), __ldcs(s + c + 2),
                                          __ldcs(s + c + 3));
             *reinterpret_cast<float4 *>(d + c) = v;
         }
-        for (int c = c4 + blockIdx.x * blockDim.x + threadIdx.x; c < cols;
-             c += gridDim.x * blockDim.x)
+        for (int c = c4 + bx * blockDim.x + threadIdx.x; c < j.cols; c += j.gx * blockDim.x)
             d[c] = s[c];
     }
 }
@@ -670,23 +694,25 @@ cudaError_t launch_packed(int inner, const SimtProblem &p, cudaStream_t stream,
             *detail = "repacking workspace allocation failed";
             return err;
         }
+        PackJob jobs[2];
+        int njobs = 0;
         if (packA) {
-            pack_rows_kernel<<<rows_grid(static_cast<long long>(p.M) * p.batch, p.K), 256, 0,
-                               stream>>>(p.A, p.lda, p.strideA, ws, ldA, elemsA, p.M, p.K,
-                                         p.batch);
+            jobs[njobs++] = pack_job(p.A, p.lda, p.strideA, ws, ldA, elemsA, p.M, p.K, p.batch);
             q.A = ws;
             q.lda = ldA;
             q.strideA = p.batch > 1 ? elemsA : 0;
         }
         if (packB) {
             float *wb = ws + elemsA * p.batch;
-            pack_rows_kernel<<<rows_grid(static_cast<long long>(p.K) * p.batch, p.N), 256, 0,
-                               stream>>>(p.B, p.ldb, p.strideB, wb, ldB, elemsB, p.K, p.N,
-                                         p.batch);
+            jobs[njobs++] = pack_job(p.B, p.ldb, p.strideB, wb, ldB, elemsB, p.K, p.N, p.batch);
             q.B = wb;
             q.ldb = ldB;
             q.strideB = p.batch > 1 ? elemsB : 0;
         }
+        long long blocks = 0;
+        for (int i = 0; i < njobs; ++i) blocks += static_cast<long long>(jobs[i].gx) * jobs[i].gy;
+        pack_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(jobs[0], jobs[njobs - 1],
+                                                                           p.batch);
         err = cudaGetLastError();
         if (err != cudaSuccess) {
             *detail = "repacking kernel launch failed";
