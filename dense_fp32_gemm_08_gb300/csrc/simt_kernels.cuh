@@ -609,8 +609,12 @@ struct TmaProducer {
 // MAXREG caps registers per thread (255 leaves room for two four-warp CTAs per SM).
 // KSUB: 32-wide k sub-tiles per pipeline stage (a stage then covers 32 * KSUB values of k,
 // with one CTA barrier and one TMA refill per stage); the TMA loader only for KSUB > 1.
+// KTAIL (KSUB > 1): the instance for K whose last stage holds padding past its first 32-wide
+// sub-tile; that stage computes only the sub-tiles that hold values of k (the rest are the
+// zeros TMA filled in). A separate instance, so the main loop of every other K keeps no
+// branch (the branch cost 0.65% at 4096^3).
 template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG,
-          int LOADER = kLoaderTma, int KSUB = 1>
+          int LOADER = kLoaderTma, int KSUB = 1, int KTAIL = 0>
 __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
     simt_gemm_persistent_kernel(const __grid_constant__ CUtensorMap mapA,
                                 const __grid_constant__ CUtensorMap mapB, const PParams p) {
@@ -709,11 +713,13 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
             }
             const float *sA = smem + s * STAGE_FLOATS;
 #pragma unroll
-            for (int j = 0; j < KSUB; ++j)
+            for (int j = 0; j < KSUB; ++j) {
+                if (KTAIL && j > 0 && kt == p.KT - 1 && p.k.K - kt * (KSUB * BK) <= j * BK) break;
                 compute_ktile<BN, (KSUB == 2 || LOADER != kLoaderTma) ? kOrderColumnSnake
                                                                       : kOrderHalfSnake>(
                     sA + j * A_SUB + (wm0 + tr) * BK, tr, sA + A_FLOATS + j * BK * BN + wn0 + 4 * tc,
                     acc);
+            }
             if (LOADER == kLoaderTma) {
                 __syncthreads();  // every warp is done with stage s
                 if (s_abort) break;
@@ -1027,7 +1033,7 @@ cudaError_t launch_impl(int id, const SimtProblem &p, cudaStream_t stream, const
 }
 
 template <int BM, int BN, int WARPS_M, int WARPS_N, int STAGES, int MAXREG = 255,
-          int LOADER = kLoaderTma, int KSUB = 1>
+          int LOADER = kLoaderTma, int KSUB = 1, int KTAIL = 0>
 cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t stream,
                               const char **detail) {
     constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
@@ -1035,7 +1041,7 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
     constexpr size_t SMEM = static_cast<size_t>(STAGES) * KSUB * (BM * BK + BK * BN) * 4 +
                             2 * STAGES * sizeof(uint64_t) + 1024;
     auto kernel =
-        simt_gemm_persistent_kernel<BM, BN, WARPS_M, WARPS_N, STAGES, MAXREG, LOADER, KSUB>;
+        simt_gemm_persistent_kernel<BM, BN, WARPS_M, WARPS_N, STAGES, MAXREG, LOADER, KSUB, KTAIL>;
 
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
