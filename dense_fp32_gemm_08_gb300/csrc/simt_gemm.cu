@@ -325,6 +325,8 @@ PackJob pack_job(const float *src, long long lds, long long ss, float *dst, long
 // unaligned source row (a warp's loads still cover 512 contiguous bytes) and one 16-byte store
 // into the aligned copy.
 __global__ void pack_rows_kernel(const PackJob j0, const PackJob j1, int batch) {
+    // the GEMM that reads the copies may start its prologue now (it waits for this grid)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     long long bid = blockIdx.x;
     const long long blocks0 = static_cast<long long>(j0.gx) * j0.gy;
     const bool first = bid < blocks0;
@@ -723,6 +725,7 @@ cudaError_t launch_packed(int inner, const SimtProblem &p, cudaStream_t stream,
         *detail = "operands not readable by TMA after repacking";
         return cudaErrorInvalidValue;
     }
+    q.pdl = packA || packB;  // the persistent kernels overlap their prologue with the copy
     return launch_config(inner, q, stream, detail);
 }
 
@@ -743,6 +746,8 @@ __global__ void apply_staged_c_kernel(const float *__restrict__ D, long long ldd
                                       float *__restrict__ C, long long ldc, long long sc,
                                       int rows, int cols, int batch, float alpha, float beta,
                                       const float *__restrict__ bias, int act) {
+    // launched as a programmatic dependent of the GEMM: D is read only once that grid is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long nrows = static_cast<long long>(rows) * batch;
     const bool fused = bias != nullptr || act != kActNone;
     for (long long gr = blockIdx.y; gr < nrows; gr += gridDim.y) {
@@ -797,12 +802,22 @@ cudaError_t launch_staged_c(int id, const SimtProblem &p, cudaStream_t stream,
     q.beta = 0.0f;
     q.bias = nullptr;
     q.act = kActNone;
+    q.pdl_next = true;  // the pass below may begin its launch while the GEMM runs
     err = launch_config(id, q, stream, detail);
     if (err != cudaSuccess) return err;
-    apply_staged_c_kernel<<<rows_grid(static_cast<long long>(p.M) * p.batch, p.N), 256, 0,
-                            stream>>>(D, ldd, elems, p.C, p.ldc, p.strideC, p.M, p.N, p.batch,
-                                      p.alpha, p.beta, p.bias, p.act);
-    err = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = rows_grid(static_cast<long long>(p.M) * p.batch, p.N);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, apply_staged_c_kernel, static_cast<const float *>(D), ldd,
+                             elems, p.C, p.ldc, p.strideC, p.M, p.N, p.batch, p.alpha, p.beta,
+                             p.bias, p.act);
+    if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) *detail = "staged-C epilogue launch failed";
     return err;
 }

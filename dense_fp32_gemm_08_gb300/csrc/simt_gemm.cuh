@@ -45,6 +45,13 @@ struct SimtProblem {
     bool transB = false;  // B stored N x K (op(B) = B^T); the tile kernels take false only
     const float *bias = nullptr;  // fused epilogue: per-column bias (N values), or none
     int act = 0;                  // fused epilogue: Activation (epilogue.cuh)
+    // The library's own chaining of kernels on one stream (programmatic dependent launch);
+    // callers leave both false. pdl: the launch follows a library kernel that lets it start
+    // early, and the persistent kernels wait for that kernel's completion before they read
+    // memory. pdl_next: a library kernel launched after this one may start early (it waits
+    // for this one's completion in the same way).
+    bool pdl = false;
+    bool pdl_next = false;
 };
 
 int simt_num_configs();

@@ -149,6 +149,7 @@ cudaError_t simt_launch_noalloc(const SimtProblem &p, cudaStream_t stream, const
     pp.ws = nullptr;
     pp.flags = nullptr;
     pp.epoch = 1;
+    pp.chain = 0;
     if (dp_tiles < T) {
         // The stream-K part needs one slot per CTA.
         if (G > kStaticSlots) {

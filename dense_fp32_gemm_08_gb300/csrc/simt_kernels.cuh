@@ -493,6 +493,7 @@ struct PParams {
     float4 *ws;           // partial sums: [G][consumer warps][32][32] float4
     unsigned int *flags;  // [G][consumer warps]
     unsigned int epoch;   // this launch's flag value (never 0)
+    int chain;            // 1: wait for the kernel before (programmatic launch), 2: let the next start
 };
 
 struct Segment {
@@ -656,6 +657,12 @@ __global__ void __launch_bounds__(WARPS_M *WARPS_N * 32) __maxnreg__(MAXREG)
     TmaProducer prod_local;
     TmaProducer &prod = LOADER == kLoaderTma ? s_prod : prod_local;
     if (LOADER != kLoaderTma || tid == 0) prod.init(p, cta);
+    // Launched as a programmatic dependent (the repacking kernel before it), the prologue above
+    // overlapped that kernel's tail; nothing below reads global memory before it has completed.
+    // The kernel after this one (the staged-C pass) may begin its launch now: it waits in the
+    // same way.
+    if (p.chain & 1) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (p.chain & 2) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
     auto produce = [&]() {
         const int s = prod.issued % STAGES;
@@ -1132,6 +1139,7 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
     pp.ws = nullptr;
     pp.flags = nullptr;
     pp.epoch = 1;
+    pp.chain = (p.pdl ? 1 : 0) | (p.pdl_next ? 2 : 0);
     if (dp_tiles < T) {
         if (G * CONSUMER_WARPS * sizeof(unsigned int) > kFlagBytes) {
             *detail = "persistent grid above the workspace's flag capacity";
@@ -1159,7 +1167,21 @@ cudaError_t launch_persistent(int schedule, const SimtProblem &p, cudaStream_t s
                      "[sgemm] persistent %dx%d: occupancy %d, grid %lld, tiles %lld, dp_tiles %lld, "
                      "k-tiles/tile %d, stream-K iters/CTA %lld (+1 for %d)\n",
                      BM, BN, occupancy[dev], G, T, dp_tiles, KT, pp.sk_base, pp.sk_rem);
-    kernel<<<static_cast<unsigned>(G), THREADS, SMEM, stream>>>(mapA, mapB, pp);
+    if (p.pdl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(G), 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = SMEM;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, kernel, mapA, mapB, pp);
+    } else {
+        kernel<<<static_cast<unsigned>(G), THREADS, SMEM, stream>>>(mapA, mapB, pp);
+    }
     err = cudaGetLastError();
     if (err != cudaSuccess) *detail = "kernel launch failed";
     return err;
