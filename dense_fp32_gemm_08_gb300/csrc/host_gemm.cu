@@ -6,9 +6,9 @@
 // GEMMs, so a long product runs at the slower of the copy rate and the kernel rate instead
 // of their sum; with pageable memory everything runs in order on the caller's stream.
 // B must be on the device before the first chunk can finish, so the first chunk is computed
-// as K slices, each starting as soon as its rows of B and columns of A have arrived (later
-// slices accumulate into C with beta = 1): the GPU starts after a quarter of B instead of
-// all of it. Every GEMM is computed by the same device entry point (the SIMT path, with its
+// as K slices of growing size, each starting as soon as its rows of B and columns of A have
+// arrived (later slices accumulate into C with beta = 1): the GPU starts after the first 256
+// rows of B instead of all of them. Every GEMM is computed by the same device entry point (the SIMT path, with its
 // per-shape configuration).
 #include <cuda_runtime.h>
 
@@ -149,9 +149,23 @@ cudaError_t host_gemm(const HostProblem &p, cudaStream_t stream, DeviceGemmFn ge
     cudaStream_t up = overlap ? h->up : stream;
     cudaStream_t down = overlap ? h->down : stream;
 
-    // The first chunk in K slices of at least 256 (multiples of 32), at most four.
-    const int kslices = reads_ab ? static_cast<int>(std::min<long long>(4, p.K / 256)) : 1;
-    const long long kc = kslices > 1 ? ((p.K + kslices - 1) / kslices + 31) / 32 * 32 : p.K;
+    // The first chunk in K slices that grow: the GPU starts once the first 256 rows of B (and
+    // that slice of A) are up, and slice i is at most 256 + 0.4 x (the K already issued), so
+    // each slice's upload (about 0.7 of its GEMM's time at 1024 x 4096 per k) lands before the
+    // GEMMs ahead of it run out. Multiples of 32; a remainder under 128 joins the last slice.
+    std::vector<long long> kslice = {0};
+    if (reads_ab && p.K >= 512) {
+        long long k = 0;
+        while (k < p.K) {
+            long long len = (256 + 2 * k / 5 + 31) / 32 * 32;
+            if (p.K - (k + len) < 128) len = p.K - k;
+            k += len;
+            kslice.push_back(k);
+        }
+    } else {
+        kslice.push_back(p.K);
+    }
+    const int kslices = static_cast<int>(kslice.size()) - 1;
 
     // The upload stream starts after everything already queued on the caller's stream.
     err = cudaEventRecord(h->caller_done, stream);
@@ -180,8 +194,8 @@ cudaError_t host_gemm(const HostProblem &p, cudaStream_t stream, DeviceGemmFn ge
                                     p.ldc * sizeof(float), p.N * sizeof(float), rows,
                                     cudaMemcpyHostToDevice, up);
         if (i == 0 && kslices > 1) {
-            for (long long k0 = 0; k0 < p.K && err == cudaSuccess; k0 += kc) {
-                const long long kn = (p.K - k0) < kc ? (p.K - k0) : kc;
+            for (int si = 0; si < kslices && err == cudaSuccess; ++si) {
+                const long long k0 = kslice[si], kn = kslice[si + 1] - kslice[si];
                 err = copy_rows(dB + k0 * ldn, ldn * sizeof(float), p.B + k0 * p.ldb,
                                         p.ldb * sizeof(float), p.N * sizeof(float), kn,
                                         cudaMemcpyHostToDevice, up);

@@ -24,8 +24,8 @@ def _host(a: np.ndarray, pinned: bool):
 @pytest.mark.parametrize("M,N,K,alpha,beta,pad", [
     (1000, 777, 555, 0.7, -1.3, 0), (100, 300, 200, 1.0, 0.0, 0), (1025, 513, 257, 1.5, 0.5, 3),
     (4096, 4096, 4096, 1.0, 0.0, 0), (300, 200, 100, 0.0, 2.0, 0),
-    # eight 512-row chunks (the last in two halves), the first in three K slices (352, 352,
-    # 296), beta != 0, padded
+    # eight 512-row chunks (the last in two halves), the first in three K slices (256, 384,
+    # 360), beta != 0, padded
     (4096, 4864, 1000, 0.7, -1.3, 5), (2049, 1023, 771, 1.0, 1.0, 1)])
 def test_host_buffers(sgemm_lib, pinned, M, N, K, alpha, beta, pad):
     A = synth.normal(M, K, 1)
