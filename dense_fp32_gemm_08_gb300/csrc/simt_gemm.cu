@@ -746,8 +746,9 @@ cudaError_t launch_packed(int inner, const SimtProblem &p, cudaStream_t stream,
 constexpr long long kStageCMinElems = 1LL << 22;
 
 // Rows over the grid's y dimension (batch entries stacked), four consecutive columns per
-// thread: one 16-byte load of D (its leading dimension is a multiple of 4; a row's last group
-// may read padding, which is allocated and unused), the C values loaded before any store.
+// thread: one 16-byte load of D (its leading dimension is a multiple of 4; a row's last,
+// partial group is read value by value, so the scratch's unwritten padding is never read),
+// the C values loaded before any store.
 __global__ void apply_staged_c_kernel(const float *__restrict__ D, long long ldd, long long sd,
                                       float *__restrict__ C, long long ldc, long long sc,
                                       int rows, int cols, int batch, float alpha, float beta,
@@ -762,9 +763,19 @@ __global__ void apply_staged_c_kernel(const float *__restrict__ D, long long ldd
         float *c = C + b * sc + r * ldc;
         for (int j = 4 * (blockIdx.x * blockDim.x + threadIdx.x); j < cols;
              j += 4 * gridDim.x * blockDim.x) {
-            const float4 v4 = __ldcs(reinterpret_cast<const float4 *>(d + j));
-            const float v[4] = {v4.x, v4.y, v4.z, v4.w};
             const int n = cols - j < 4 ? cols - j : 4;
+            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (n == 4) {
+                const float4 v4 = __ldcs(reinterpret_cast<const float4 *>(d + j));
+                v[0] = v4.x;
+                v[1] = v4.y;
+                v[2] = v4.z;
+                v[3] = v4.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (e < n) v[e] = d[j + e];
+            }
             float cv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int e = 0; e < 4; ++e)

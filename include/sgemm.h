@@ -17,9 +17,9 @@
  *   torch CUDA tensors). The library keeps no reference to them after the call returns.
  *   No entry point allocates device memory on every call: workspaces are allocated on first
  *   use (per device and stream: stream-K and split-K partial sums, repacked or transposed
- *   operand copies, the 3xTF32 / TF32 split operands; per device: the host-memory path's
- *   buffers), grown when a larger problem needs more, and kept until
- *   sgemm_release_workspace(). sgemm_noalloc() uses none of them.
+ *   operand copies, the staged product of an unaligned C, the 3xTF32 / TF32 split operands;
+ *   per device: the host-memory path's buffers), grown when a larger problem needs more, and
+ *   kept until sgemm_release_workspace(). sgemm_noalloc() uses none of them.
  * Streams: every compute call is asynchronous on `stream` (a cudaStream_t; NULL means the
  *   legacy default stream) and does not synchronise. Results are visible to later work on
  *   the same stream.
@@ -90,6 +90,11 @@ typedef enum sgemm_activation {
  *   C         M x N, ldc >= max(1, N).
  *   A, B may be NULL only when alpha == 0 or K == 0; C may be NULL only when M or N is 0.
  *   stream    cudaStream_t or NULL.
+ * Any alignment. When C's rows are not 16-byte aligned (an ldc that is not a multiple of 4, or
+ * a misaligned C), beta != 0 and M * N is at least 2^22, the product is computed into an
+ * aligned workspace of 4 * M * N' bytes (N' = N rounded up to a multiple of 4) and a second
+ * pass applies alpha, beta (and, for sgemm_fused on this path, the bias and activation) to C:
+ * the same fp32 arithmetic as the single-pass epilogue, so the result is the same bit for bit.
  */
 sgemm_status_t sgemm(int64_t M, int64_t N, int64_t K, float alpha,
                      const float *A, int64_t lda, const float *B, int64_t ldb,
@@ -240,11 +245,11 @@ sgemm_status_t sgemm_fused_strided_batched(sgemm_op_t transa, sgemm_op_t transb,
  * The product with A, B and C in HOST memory (same sizes, leading dimensions, alpha / beta
  * rules and argument errors as sgemm()). The call returns when C holds the result. B is
  * uploaded once; the rows of A (and of C when beta != 0) travel in chunks (at least M / 8
- * rows, grown until a chunk fills the GPU with tiles) through two device buffers each,
+ * rows, grown until a chunk holds half a wave of tiles) through two device buffers each,
  * uploaded on an internal stream while the previous chunk is computed on `stream` (the SIMT
  * path) and the one before it is downloaded on another internal stream. The first chunk is
- * computed in up to four K slices, each starting when its part of B has arrived (the slices
- * accumulate in fp32, like stream-K pieces). With pinned (page-locked) host memory the copies
+ * computed in K slices of growing size (256, 384, 512, ... rows of B), each starting when its
+ * part of B has arrived (the slices accumulate in fp32, like stream-K pieces). With pinned (page-locked) host memory the copies
  * overlap the computation; pageable memory works but the copies then serialise. Device
  * buffers of about 4 * (K * N + 2 * chunk * (K + N)) bytes (rows padded to 16 bytes) are kept
  * per device until sgemm_release_workspace(); calls on the same device run one at a time.
