@@ -381,6 +381,36 @@ def pin_epilogue_transposed(lib):
     return True
 
 
+
+def pin_page_counts(lib):
+    """The counts the pages print for the 4096^3 problem (tests/golden/headline_counts.json):
+    from the definition (2 n^3 FLOP, n^2 outputs, 3 n^2 four-byte inputs, their ratio), and
+    through the oracle: an output cell sums exactly n products (A row and B all ones give
+    C = n in every cell of the row), and one element of A reaches exactly n output cells (a
+    single nonzero A[i0][k0] with B all ones fills row i0 and no other row)."""
+    import json
+    from pathlib import Path
+    g = json.loads((Path(__file__).parent / "golden" / "headline_counts.json").read_text())
+    n, pr = g["n"], g["printed"]
+    ok = round(2 * n ** 3 / 1e9) == pr["flop_billions"]
+    ok &= (n * n // 100_000) / 10 == pr["outputs_millions"]  # 16.78 million, printed cut to 16.7
+    ok &= round(3 * n * n * 4 / 1e6) == pr["input_megabytes"]
+    ok &= round(2 * n ** 3 / (3 * n * n * 4) / 10) * 10 == pr["flop_per_byte"]
+    B = np.ones((n, n), np.float32)
+    i0, k0, other = 1234, 777, 4095
+    A = np.zeros((n, n), np.float32)
+    A[i0, :] = 1.0
+    rows = [i0, other]
+    C = _mm(lib, n, n, n, 1.0, A, n, B, n, 0.0, None, n, rows=rows)
+    ok &= bool(np.all(C[0] == pr["multiply_adds_per_output"]))
+    ok &= bool(np.all(C[1] == 0.0))
+    A[:] = 0.0
+    A[i0, k0] = 1.0
+    C = _mm(lib, n, n, n, 1.0, A, n, B, n, 0.0, None, n, rows=rows)
+    ok &= int(np.count_nonzero(C[0])) == pr["output_cells_per_element_of_A"]
+    ok &= int(np.count_nonzero(C[1])) == 0
+    return bool(ok)
+
 PINS = {
     "identity": pin_identity,
     "permutation": pin_permutation,
@@ -398,4 +428,5 @@ PINS = {
     "epilogue_bias_and_residual": pin_epilogue_bias_and_residual,
     "epilogue_transposed": pin_epilogue_transposed,
     "absdot": pin_absdot,
+    "page_counts": pin_page_counts,
 }
