@@ -783,13 +783,21 @@ def measure_sweep(torch, sg, dev, stream, flush, sms, steps):
 def launches_per_call(path: str, kernel: str, w) -> int:
     """Kernels one library call launches for the bench's operands (lda = K, ldb = N,
     ldc = N, 16-byte-aligned allocations): the tensor paths split (or round) both operands in
-    one launch, then run the GEMM; a repacked SIMT configuration first copies each operand
-    whose rows TMA cannot read (K or N not a multiple of 4) into aligned storage."""
+    one launch, then run the GEMM. On the SIMT path a repacked configuration first copies the
+    operands whose rows TMA cannot read (K or N not a multiple of 4) into aligned storage, in
+    one launch; and when C's rows are not 16-byte aligned (N not a multiple of 4), beta != 0
+    and the call has at least 2^22 outputs, a tile kernel's product goes to an aligned scratch
+    and one more launch applies the epilogue to C (the skinny and small-problem kernels read C
+    themselves)."""
     if path in ("3xtf32", "tf32"):
         return 2
     n = 1
-    if kernel.startswith("packed"):
-        n += int(w["K"] % 4 != 0) + int(w["N"] % 4 != 0)
+    if kernel.startswith("packed") and (w["K"] % 4 != 0 or w["N"] % 4 != 0):
+        n += 1
+    tile_kernel = not kernel.startswith(("skinny", "splitk"))
+    if (tile_kernel and w.get("beta", 0.0) != 0.0 and w["N"] % 4 != 0
+            and w["M"] * w["N"] >= 1 << 22):
+        n += 1
     return n
 
 

@@ -168,10 +168,14 @@ def test_nvml_sampler_without_a_driver_reports_no_samples():
 
 
 def test_launches_per_call():
-    w = {"M": 4095, "N": 3001, "K": 1537}
+    edge0 = bench.WORKLOADS["edge0"]  # 4095 x 3001 x 1537, beta = -1.3: repack + GEMM + C pass
     assert bench.launches_per_call("simt", "sk_tma_ws_128x256_k64_s2", bench.WORKLOADS["headline"]) == 1
-    assert bench.launches_per_call("simt", "packed_sk_tma_128x256_s4", w) == 3
-    assert bench.launches_per_call("3xtf32", "tf32x3_tcgen05", w) == 2
+    assert bench.launches_per_call("simt", "packed_sk_tma_256x128_k64_s2", edge0) == 3
+    assert bench.launches_per_call("simt", "packed_sk_tma_256x128_k64_s2", dict(edge0, beta=0.0)) == 2
+    small = {"M": 127, "N": 129, "K": 4099, "beta": -1.3}  # under 2^22 outputs: C read in place
+    assert bench.launches_per_call("simt", "splitk_cpasync_64x64", small) == 1
+    assert bench.launches_per_call("simt", "skinny_wide_m8", bench.WORKLOADS["edge1"]) == 1
+    assert bench.launches_per_call("3xtf32", "tf32x3_tcgen05", edge0) == 2
 
 
 def test_oracle_sizes_are_bounded_and_labelled():
