@@ -69,6 +69,16 @@ def test_transposed_large(sgemm_lib):
     _run(sgemm_lib, "simt", True, True, 2048, 2048, 2048, 1.0, 0.0, seed=5)
 
 
+@pytest.mark.parametrize("ta,tb", [(True, False), (False, True)])
+def test_transposed_unaligned_c_staged(sgemm_lib, ta, tb):
+    # ldc = N = 2051 (odd), beta != 0 and 4.2 M outputs: the untransposed product is staged in
+    # an aligned scratch and a second pass applies alpha and beta to C
+    _run(sgemm_lib, "simt", ta, tb, 2049, 2051, 300, 0.7, -1.3, seed=7)
+    got, ref = _run(sgemm_lib, "simt", ta, tb, 2049, 2051, 300, 1.0, 2.0, dist="small_int",
+                    seed=8)
+    assert np.array_equal(got, ref)
+
+
 @pytest.mark.parametrize("path", ["simt", "3xtf32"])
 def test_transposed_strided_batched(sgemm_lib, path):
     sg = sgemm_lib
